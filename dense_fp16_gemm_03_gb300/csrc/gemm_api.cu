@@ -1,0 +1,539 @@
+// C ABI of the fp16 NT GEMM (declared in include/gemm_f16.h): argument
+// validation, planning (variant, raster width, grid), TMA tensor-map
+// encoding, and the launch of the persistent sm_103a kernel.
+//
+// The interface mirrors the call of "1. WGMMA: Hopper's Asynchronous Tensor
+// Core" (section "The Full Kernel": m, n, k and the a, b, c fp16 pointers)
+// plus a stream, a plan query and a workspace query.  The capability gate
+// answers the one on the "wgmma_gemm.cu" page (refuse a device the code was
+// not built for with a clear status instead of failing inside the driver).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string.h>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+
+using namespace gemm_f16;
+
+// The device error word: set by a kernel whose pipeline wait timed out,
+// read and cleared by gemm_f16_take_device_error.
+__device__ uint32_t g_gemm_f16_error_word = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// ------------------------------------------------------------ variants
+
+struct Variant {
+    int cg, bn, stages, smem;
+    const void *fn;
+    cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
+};
+
+template <int CG, int BN, int ST>
+cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(unsigned(plan.grid), 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST>::kSmemBytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        na = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST>, params);
+}
+
+#define GEMM_VARIANT(CG, BN, ST)                                                                 \
+    Variant                                                                                      \
+    {                                                                                            \
+        CG, BN, ST, KernelCfg<CG, BN, ST>::kSmemBytes,                                           \
+            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST>), &launch_variant<CG, BN, ST> \
+    }
+
+const Variant kVariants[] = {
+    GEMM_VARIANT(1, 256, 4),  // 0: 128 x 256 tile, one CTA
+    GEMM_VARIANT(1, 128, 6),  // 1: 128 x 128 tile, one CTA
+    GEMM_VARIANT(2, 256, 6),  // 2: 256 x 256 tile on a CTA pair
+    GEMM_VARIANT(2, 128, 8),  // 3: 256 x 128 tile on a CTA pair
+};
+constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
+
+// ---------------------------------------------------- per-device state
+
+struct DeviceInfo {
+    bool ready = false;
+    bool arch_ok = false;
+    int num_sms = 0;
+    int max_clusters[kNumVariants] = {};
+    bool attr_set[kNumVariants] = {};
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+gemm_status_t device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        d.arch_ok = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.arch_ok) {
+            for (int v = 0; v < kNumVariants; ++v) {
+                const Variant &var = kVariants[v];
+                if (cudaFuncSetAttribute(var.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, var.smem) !=
+                    cudaSuccess) {
+                    cudaGetLastError();
+                    return GEMM_ERR_CUDA;
+                }
+                d.attr_set[v] = true;
+                d.max_clusters[v] = sms / var.cg;
+                if (var.cg == 2) {
+                    cudaLaunchConfig_t cfg;
+                    memset(&cfg, 0, sizeof(cfg));
+                    cfg.gridDim = dim3(unsigned(2 * (sms / 2)), 1, 1);
+                    cfg.blockDim = dim3(kNumThreads, 1, 1);
+                    cfg.dynamicSmemBytes = size_t(var.smem);
+                    cudaLaunchAttribute attr;
+                    attr.id = cudaLaunchAttributeClusterDimension;
+                    attr.val.clusterDim.x = 2;
+                    attr.val.clusterDim.y = 1;
+                    attr.val.clusterDim.z = 1;
+                    cfg.attrs = &attr;
+                    cfg.numAttrs = 1;
+                    int clusters = 0;
+                    if (cudaOccupancyMaxActiveClusters(&clusters, var.fn, &cfg) == cudaSuccess && clusters > 0)
+                        d.max_clusters[v] = clusters;
+                    else
+                        cudaGetLastError();
+                }
+            }
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return d.arch_ok ? GEMM_OK : GEMM_ERR_ARCH;
+}
+
+// ---------------------------------------------------------- validation
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+gemm_status_t check_shape(int64_t m, int64_t n, int64_t k)
+{
+    if (m < 0 || n < 0 || k < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t lim = int64_t(1) << 31;
+    if (m >= lim || n >= lim || k >= lim) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (k % 8 != 0 || n % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    return GEMM_OK;
+}
+
+gemm_status_t check_pointers(int64_t m, int64_t n, int64_t k, const void *a, const void *b, const void *c)
+{
+    if (m > 0 && n > 0) {
+        if (!c) return GEMM_ERR_INVALID_ARG;
+        if (!aligned16(c)) return GEMM_ERR_ALIGNMENT;
+        if (k > 0) {
+            if (!a || !b) return GEMM_ERR_INVALID_ARG;
+            if (!aligned16(a) || !aligned16(b)) return GEMM_ERR_ALIGNMENT;
+        }
+    }
+    return GEMM_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b)
+{
+    return (a + b - 1) / b;
+}
+
+// --------------------------------------------------------------- plans
+
+// Raster width: enough N-columns per group that a wave of concurrently
+// running tiles forms a roughly square block of the tile grid.
+int32_t auto_raster_width(int64_t tiles_m, int64_t tiles_n, int64_t slots)
+{
+    int64_t w = 1;
+    while (w * w < slots && w < tiles_n) w *= 2;
+    if (w > tiles_n) w = tiles_n;
+    (void)tiles_m;
+    return int32_t(w < 1 ? 1 : w);
+}
+
+// Tile-shape choice: among the compiled variants, minimise the number of
+// full waves of tiles over the resident CTA slots, weighted by the work of
+// one tile; ties go to the larger tile (less operand traffic per flop).
+int32_t auto_variant(int64_t m, int64_t n, int32_t num_sms, int32_t max_clusters)
+{
+    int best = 0;
+    double best_cost = 0.0;
+    for (int v = 0; v < kNumVariants; ++v) {
+        const Variant &var = kVariants[v];
+        const int64_t bm = 128 * var.cg;
+        const int64_t tiles = cdiv(m, bm) * cdiv(n, var.bn);
+        int64_t slots = (var.cg == 2) ? (max_clusters > 0 ? max_clusters : num_sms / 2) : num_sms;
+        if (slots < 1) slots = 1;
+        const int64_t waves = cdiv(tiles, slots);
+        // time ~ waves x (tile work / per-slot throughput); a pair has twice the tensor cores
+        const double tile_work = double(bm) * double(var.bn) / double(var.cg);
+        // larger tiles re-read less: small penalty per unit of operand traffic per flop
+        const double traffic = 1.0 / double(bm) + 1.0 / double(var.bn);
+        const double cost = double(waves) * tile_work * (1.0 + 8.0 * traffic);
+        if (v == 0 || cost < best_cost * 0.999) {
+            best = v;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters_in,
+                        int32_t variant, int32_t raster_width, int32_t split_k, gemm_f16_plan_t *out)
+{
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
+    if (variant >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+    if (split_k > 1) return GEMM_ERR_INVALID_ARG;  // no split-K kernel in this build
+    const int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / 2;
+    if (variant < 0) variant = auto_variant(m, n, num_sms, max_clusters);
+    const Variant &var = kVariants[variant];
+    gemm_f16_plan_t p;
+    memset(&p, 0, sizeof(p));
+    p.variant = variant;
+    p.cta_group = var.cg;
+    p.block_m = 128 * var.cg;
+    p.block_n = var.bn;
+    p.block_k = kBlockK;
+    p.stages = var.stages;
+    p.split_k = 1;
+    p.m = m;
+    p.n = n;
+    p.k = k;
+    p.tiles_m = cdiv(m, p.block_m);
+    p.tiles_n = cdiv(n, p.block_n);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.k_blocks = cdiv(k, kBlockK);
+    p.cluster = var.cg;
+    p.smem_bytes = var.smem;
+    p.num_sms = num_sms;
+    p.workspace_bytes = 0;
+    int64_t slots = (var.cg == 2) ? max_clusters : num_sms;
+    if (slots < 1) slots = 1;
+    const int64_t clusters = p.num_tiles < slots ? p.num_tiles : slots;
+    p.grid = int32_t(clusters * var.cg);
+    if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_m, p.tiles_n, slots);
+    if (p.tiles_n > 0 && raster_width > p.tiles_n) raster_width = int32_t(p.tiles_n);
+    if (raster_width < 1) raster_width = 1;
+    p.raster_width = raster_width;
+    if (p.num_tiles >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    *out = p;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+gemm_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
+{
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    *fn = g_encode;
+    return g_encode ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Row-major fp16 matrix of `rows` x `cols` (cols contiguous), 128-byte
+// swizzled boxes of box_cols x box_rows, zero fill outside the matrix.
+gemm_status_t encode_matrix(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *ptr,
+                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+}
+
+gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b, void *c, void *ws,
+                       size_t ws_bytes, cudaStream_t stream, uint32_t skip_fill, long long wait_limit)
+{
+    gemm_status_t st = check_shape(plan.m, plan.n, plan.k);
+    if (st != GEMM_OK) return st;
+    st = check_pointers(plan.m, plan.n, plan.k, a, b, c);
+    if (st != GEMM_OK) return st;
+    if (plan.m == 0 || plan.n == 0) return GEMM_OK;
+    if (plan.workspace_bytes > 0 && (ws == nullptr || ws_bytes < plan.workspace_bytes)) return GEMM_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    if (plan.k == 0) {
+        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * 2u, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
+    // the plan must be one this library would make: re-derive and compare
+    gemm_f16_plan_t check;
+    st = make_plan(plan.m, plan.n, plan.k, plan.num_sms, 0, plan.variant, plan.raster_width, plan.split_k, &check);
+    if (st != GEMM_OK) return st;
+    // (any grid of whole clusters is correct: the kernel walks the tiles persistently)
+    if (check.variant != plan.variant || check.tiles_m != plan.tiles_m || check.tiles_n != plan.tiles_n ||
+        check.k_blocks != plan.k_blocks || check.smem_bytes != plan.smem_bytes || plan.cluster != check.cluster ||
+        plan.grid < plan.cluster || plan.grid % plan.cluster != 0 || plan.grid / plan.cluster > plan.num_tiles)
+        return GEMM_ERR_INVALID_ARG;
+    const Variant &var = kVariants[plan.variant];
+
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    st = get_encoder(&enc);
+    if (st != GEMM_OK) return st;
+    KernelParams params;
+    memset(&params, 0, sizeof(params));
+    st = encode_matrix(enc, &params.tmap_a, a, uint64_t(plan.m), uint64_t(plan.k), kBlockK, 128);
+    if (st != GEMM_OK) return st;
+    st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.n), uint64_t(plan.k), kBlockK,
+                       uint32_t(var.bn / var.cg));
+    if (st != GEMM_OK) return st;
+    st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
+    if (st != GEMM_OK) return st;
+    params.raster = make_raster(uint32_t(plan.tiles_m), uint32_t(plan.tiles_n), uint32_t(plan.raster_width));
+    params.m = uint32_t(plan.m);
+    params.n = uint32_t(plan.n);
+    params.k = uint32_t(plan.k);
+    params.num_tiles = uint32_t(plan.num_tiles);
+    params.k_blocks = uint32_t(plan.k_blocks);
+    params.skip_fill = skip_fill;
+    params.wait_limit = wait_limit;
+    void *err_ptr = nullptr;
+    if (cudaGetSymbolAddress(&err_ptr, g_gemm_f16_error_word) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    params.error_word = static_cast<uint32_t *>(err_ptr);
+    if (var.launch(plan, params, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+// A wait may legitimately last one whole tile's main loop: allow ~1 s plus
+// a generous per-K-block allowance.
+long long default_wait_limit(int64_t k_blocks)
+{
+    return 2000000000LL + k_blocks * 65536LL;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gemm_f16_status_string(gemm_status_t s)
+{
+    switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case GEMM_ERR_UNSUPPORTED_SHAPE: return "GEMM_ERR_UNSUPPORTED_SHAPE: k and n must be multiples of 8, sizes < 2^31";
+    case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_WORKSPACE: return "GEMM_ERR_WORKSPACE: workspace missing or too small";
+    case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a pipeline wait in the kernel timed out";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime call failed";
+    }
+    return "unknown gemm_status_t";
+}
+
+int32_t gemm_f16_variant_count(void)
+{
+    return kNumVariants;
+}
+
+gemm_status_t gemm_f16_variant_info(int32_t v, int32_t *cta_group, int32_t *block_n, int32_t *stages,
+                                    int32_t *smem_bytes)
+{
+    if (v < 0 || v >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+    if (cta_group) *cta_group = kVariants[v].cg;
+    if (block_n) *block_n = kVariants[v].bn;
+    if (stages) *stages = kVariants[v].stages;
+    if (smem_bytes) *smem_bytes = kVariants[v].smem;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters,
+                                   int32_t variant, int32_t raster_width, int32_t split_k, gemm_f16_plan_t *out)
+{
+    return make_plan(m, n, k, num_sms, max_clusters, variant, raster_width, split_k, out);
+}
+
+gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t *out)
+{
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != GEMM_OK) return st;
+    const int32_t auto_v = auto_variant(m, n, dev->num_sms, dev->max_clusters[2]);
+    return make_plan(m, n, k, dev->num_sms, dev->max_clusters[auto_v], auto_v, 0, 1, out);
+}
+
+gemm_status_t gemm_f16_nt_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes)
+{
+    if (!bytes) return GEMM_ERR_INVALID_ARG;
+    gemm_f16_plan_t p;
+    gemm_status_t st = gemm_f16_nt_plan(m, n, k, &p);
+    if (st != GEMM_OK) return st;
+    *bytes = size_t(p.workspace_bytes);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *c,
+                             void *workspace, size_t ws_bytes, gemm_stream_t stream)
+{
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    st = check_pointers(m, n, k, a, b, c);
+    if (st != GEMM_OK) return st;
+    if (m == 0 || n == 0) return GEMM_OK;
+    gemm_f16_plan_t p;
+    st = gemm_f16_nt_plan(m, n, k, &p);
+    if (st != GEMM_OK) return st;
+    return run_plan(p, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                    default_wait_limit(p.k_blocks));
+}
+
+gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *c,
+                          gemm_stream_t stream)
+{
+    return gemm_f16_nt_ws(m, n, k, a, b, c, nullptr, 0, stream);
+}
+
+gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c, void *workspace,
+                              size_t ws_bytes, gemm_stream_t stream)
+{
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    return run_plan(*plan, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                    default_wait_limit(plan->k_blocks));
+}
+
+// Failure-detection hook: the producer of CTA 0 leaves fill number
+// `skip_fill` undone and waits are limited to `wait_limit_cycles`, so the
+// kernel's bounded waits expire and report GEMM_ERR_TIMEOUT through
+// gemm_f16_take_device_error.
+gemm_status_t gemm_f16_nt_run_stall_test(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c,
+                                         uint32_t skip_fill, long long wait_limit_cycles, gemm_stream_t stream)
+{
+    if (!plan || wait_limit_cycles <= 0) return GEMM_ERR_INVALID_ARG;
+    return run_plan(*plan, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream), skip_fill,
+                    wait_limit_cycles);
+}
+
+gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_host, const void *b_host,
+                               void *c_host, void *a_dev, void *b_dev, void *c_dev, gemm_stream_t stream)
+{
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    st = check_pointers(m, n, k, a_dev, b_dev, c_dev);
+    if (st != GEMM_OK) return st;
+    if (m == 0 || n == 0) return GEMM_OK;
+    if (!c_host || (k > 0 && (!a_host || !b_host))) return GEMM_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (k > 0) {
+        if (cudaMemcpyAsync(a_dev, a_host, size_t(m) * size_t(k) * 2u, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(b_dev, b_host, size_t(n) * size_t(k) * 2u, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+    }
+    st = gemm_f16_nt(m, n, k, a_dev, b_dev, c_dev, stream);
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpyAsync(c_host, c_dev, size_t(m) * size_t(n) * 2u, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_take_device_error(gemm_stream_t stream, uint32_t *code)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    const uint32_t zero = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpyFromSymbol(&word, g_gemm_f16_error_word, sizeof(word)) != cudaSuccess ||
+        (word != 0 && cudaMemcpyToSymbol(g_gemm_f16_error_word, &zero, sizeof(zero)) != cudaSuccess)) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (code) *code = word;
+    return word ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+gemm_status_t gemm_f16_raster_coord(int64_t tiles_m, int64_t tiles_n, int32_t raster_width, int64_t tile,
+                                    int64_t *m_block, int64_t *n_block)
+{
+    if (!m_block || !n_block || tiles_m < 1 || tiles_n < 1 || raster_width < 1) return GEMM_ERR_INVALID_ARG;
+    if (tiles_m * tiles_n >= (int64_t(1) << 31) || tile < 0 || tile >= tiles_m * tiles_n)
+        return GEMM_ERR_INVALID_ARG;
+    Raster r = make_raster(uint32_t(tiles_m), uint32_t(tiles_n), uint32_t(raster_width));
+    uint32_t mb, nb;
+    raster_coord(r, uint32_t(tile), mb, nb);
+    *m_block = mb;
+    *n_block = nb;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_fast_divmod(uint32_t d, uint32_t n, uint32_t *q, uint32_t *r)
+{
+    if (d == 0 || !q || !r) return GEMM_ERR_INVALID_ARG;
+    FastDiv f = make_fastdiv(d);
+    *q = fast_div(f, n);
+    *r = n - *q * d;
+    return GEMM_OK;
+}
+
+}  // extern "C"

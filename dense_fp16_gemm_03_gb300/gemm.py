@@ -1,0 +1,242 @@
+"""ctypes binding of the C ABI in include/gemm_f16.h (same entry-point names).
+
+Argument marshalling only: every step of the product runs in the CUDA
+library.  A missing library raises at load time; there is no fallback.
+Device buffers are torch tensors (or raw integer device addresses); streams
+are torch.cuda.Stream objects, raw cudaStream_t integers, or None for the
+current torch stream.
+"""
+import ctypes
+import os
+
+from . import build as _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_ALIGNMENT = 2
+GEMM_ERR_UNSUPPORTED_SHAPE = 3
+GEMM_ERR_ARCH = 4
+GEMM_ERR_WORKSPACE = 5
+GEMM_ERR_LAUNCH = 6
+GEMM_ERR_TIMEOUT = 7
+GEMM_ERR_CUDA = 8
+
+LIB_PATH = _build.LIB
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+class Plan(ctypes.Structure):
+    """Mirror of gemm_f16_plan_t."""
+    _fields_ = [
+        ("variant", ctypes.c_int32),
+        ("cta_group", ctypes.c_int32),
+        ("block_m", ctypes.c_int32),
+        ("block_n", ctypes.c_int32),
+        ("block_k", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
+        ("raster_width", ctypes.c_int32),
+        ("split_k", ctypes.c_int32),
+        ("m", ctypes.c_int64),
+        ("n", ctypes.c_int64),
+        ("k", ctypes.c_int64),
+        ("tiles_m", ctypes.c_int64),
+        ("tiles_n", ctypes.c_int64),
+        ("num_tiles", ctypes.c_int64),
+        ("k_blocks", ctypes.c_int64),
+        ("grid", ctypes.c_int32),
+        ("cluster", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_uint64),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+    def __repr__(self):
+        return "Plan(%s)" % ", ".join("%s=%s" % kv for kv in self.as_dict().items())
+
+
+# every symbol the public header declares
+EXPORTED = [
+    "gemm_f16_status_string", "gemm_f16_variant_count", "gemm_f16_variant_info",
+    "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_workspace_size",
+    "gemm_f16_nt", "gemm_f16_nt_ws", "gemm_f16_nt_run", "gemm_f16_nt_host",
+    "gemm_f16_take_device_error", "gemm_f16_raster_coord", "gemm_f16_fast_divmod",
+    "gemm_f16_nt_run_stall_test",
+]
+
+_lib = None
+
+
+def lib():
+    """Load libgemm_f16.so (built in-tree by build.py); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libgemm_f16.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    i32, i64, u32, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
+    pi32, pi64, pu32 = ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(u32)
+    P = ctypes.POINTER(Plan)
+    sig = {
+        "gemm_f16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "gemm_f16_variant_count": (i32, []),
+        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32]),
+        "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),
+        "gemm_f16_nt_plan_for": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, P]),
+        "gemm_f16_nt_workspace_size": (ctypes.c_int, [i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]),
+        "gemm_f16_nt": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp]),
+        "gemm_f16_nt_ws": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
+        "gemm_f16_nt_run": (ctypes.c_int, [P, vp, vp, vp, vp, ctypes.c_size_t, vp]),
+        "gemm_f16_nt_host": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_f16_take_device_error": (ctypes.c_int, [vp, pu32]),
+        "gemm_f16_raster_coord": (ctypes.c_int, [i64, i64, i32, i64, pi64, pi64]),
+        "gemm_f16_fast_divmod": (ctypes.c_int, [u32, u32, pu32, pu32]),
+        "gemm_f16_nt_run_stall_test": (ctypes.c_int, [P, vp, vp, vp, u32, ctypes.c_longlong, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(status):
+    return lib().gemm_f16_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != GEMM_OK:
+        raise GemmError(status, where)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------- queries
+
+def gemm_f16_variant_count():
+    return int(lib().gemm_f16_variant_count())
+
+
+def gemm_f16_variant_info(variant):
+    cg, bn, st, sm = (ctypes.c_int32() for _ in range(4))
+    _check(lib().gemm_f16_variant_info(variant, ctypes.byref(cg), ctypes.byref(bn), ctypes.byref(st),
+                                       ctypes.byref(sm)), "gemm_f16_variant_info")
+    return {"cta_group": cg.value, "block_n": bn.value, "stages": st.value, "smem_bytes": sm.value}
+
+
+def gemm_f16_nt_plan(m, n, k):
+    p = Plan()
+    _check(lib().gemm_f16_nt_plan(m, n, k, ctypes.byref(p)), "gemm_f16_nt_plan")
+    return p
+
+
+def gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters=0, variant=-1, raster_width=0, split_k=0):
+    p = Plan()
+    _check(lib().gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters, variant, raster_width, split_k,
+                                      ctypes.byref(p)), "gemm_f16_nt_plan_for")
+    return p
+
+
+def gemm_f16_nt_workspace_size(m, n, k):
+    b = ctypes.c_size_t()
+    _check(lib().gemm_f16_nt_workspace_size(m, n, k, ctypes.byref(b)), "gemm_f16_nt_workspace_size")
+    return b.value
+
+
+# ------------------------------------------------------------------ launches
+
+def _shape(a, b):
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("a must be [M,K] and b [N,K]")
+    import torch
+    for t in (a, b):
+        if t.dtype != torch.float16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("operands must be contiguous float16 CUDA tensors")
+    return a.shape[0], b.shape[0], a.shape[1]
+
+
+def gemm_f16_nt(a, b, c=None, stream=None):
+    """C = A . B^T for contiguous fp16 CUDA tensors A [M,K], B [N,K]; returns C [M,N]."""
+    import torch
+    m, n, k = _shape(a, b)
+    if c is None:
+        c = torch.empty((m, n), dtype=torch.float16, device=a.device)
+    elif tuple(c.shape) != (m, n) or c.dtype != torch.float16 or not c.is_contiguous():
+        raise ValueError("c must be a contiguous float16 [M,N] tensor")
+    _check(lib().gemm_f16_nt(m, n, k, _ptr(a), _ptr(b), _ptr(c), _stream(stream)), "gemm_f16_nt")
+    return c
+
+
+def gemm_f16_nt_ws(a, b, c, workspace, stream=None):
+    m, n, k = _shape(a, b)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().gemm_f16_nt_ws(m, n, k, _ptr(a), _ptr(b), _ptr(c), _ptr(workspace), ws_bytes,
+                                _stream(stream)), "gemm_f16_nt_ws")
+    return c
+
+
+def gemm_f16_nt_run(plan, a, b, c, workspace=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().gemm_f16_nt_run(ctypes.byref(plan), _ptr(a), _ptr(b), _ptr(c), _ptr(workspace), ws_bytes,
+                                 _stream(stream)), "gemm_f16_nt_run")
+    return c
+
+
+def gemm_f16_nt_host(a_host, b_host, c_host, a_dev, b_dev, c_dev, stream=None):
+    """End-to-end call on host tensors (pinned for asynchronous copies)."""
+    m, k = a_host.shape
+    n = b_host.shape[0]
+    _check(lib().gemm_f16_nt_host(m, n, k, _ptr(a_host), _ptr(b_host), _ptr(c_host), _ptr(a_dev), _ptr(b_dev),
+                                  _ptr(c_dev), _stream(stream)), "gemm_f16_nt_host")
+    return c_host
+
+
+def gemm_f16_take_device_error(stream=None):
+    """(status, code): GEMM_ERR_TIMEOUT with the recorded code if a kernel gave up a wait."""
+    code = ctypes.c_uint32()
+    st = lib().gemm_f16_take_device_error(_stream(stream), ctypes.byref(code))
+    return st, code.value
+
+
+def gemm_f16_nt_run_stall_test(plan, a, b, c, skip_fill, wait_limit_cycles, stream=None):
+    return lib().gemm_f16_nt_run_stall_test(ctypes.byref(plan), _ptr(a), _ptr(b), _ptr(c), skip_fill,
+                                            wait_limit_cycles, _stream(stream))
+
+
+# ------------------------------------------------------ scheduler arithmetic
+
+def gemm_f16_raster_coord(tiles_m, tiles_n, raster_width, tile):
+    mb, nb = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().gemm_f16_raster_coord(tiles_m, tiles_n, raster_width, tile, ctypes.byref(mb), ctypes.byref(nb)),
+           "gemm_f16_raster_coord")
+    return mb.value, nb.value
+
+
+def gemm_f16_fast_divmod(d, n):
+    q, r = ctypes.c_uint32(), ctypes.c_uint32()
+    _check(lib().gemm_f16_fast_divmod(d, n, ctypes.byref(q), ctypes.byref(r)), "gemm_f16_fast_divmod")
+    return q.value, r.value

@@ -1,0 +1,191 @@
+/*
+ * gemm_f16.h -- C ABI of the GB300 (sm_103a) dense fp16 GEMM
+ *
+ *     C[M,N] = A[M,K] . B[N,K]^T      fp16 operands, fp32 accumulation, fp16 result
+ *
+ * The operation is the one computed by "1. WGMMA: Hopper's Asynchronous Tensor
+ * Core" (tilus tutorial), section "The Full Kernel": A is an [m, k] row-major
+ * fp16 matrix, B an [n, k] row-major fp16 matrix used transposed, the
+ * accumulator is fp32 and is cast to fp16 on the store to the [m, n]
+ * row-major C.  The output cast rounds to nearest even.
+ *
+ * Layout: every matrix is row-major and densely packed (leading dimension =
+ * number of columns): A has K contiguous elements per row, B has K contiguous
+ * elements per row (it is "K-major", i.e. B^T is column-major), C has N
+ * contiguous elements per row.
+ *
+ * Ownership: the caller owns every buffer (a, b, c, workspace) and the
+ * stream.  The library never allocates or frees device memory and keeps no
+ * per-call state; its only device-resident state is one 32-bit error word
+ * per device (see gemm_f16_take_device_error).  Launches are asynchronous
+ * on `stream`; a, b are only read; c is fully overwritten (no beta, no
+ * accumulate).  Overlap of c with a or b is undefined.
+ *
+ * Errors: every entry point validates its arguments on the host before any
+ * launch and returns a status code; it never exits or aborts the process.
+ *   - m, n, k >= 0.  m == 0 or n == 0 is a no-op.  k == 0 writes C := 0
+ *     (the empty sum) with an asynchronous memset on `stream`.
+ *   - a, b, c must be non-null and 16-byte aligned when their size is > 0
+ *     (GEMM_ERR_INVALID_ARG / GEMM_ERR_ALIGNMENT).
+ *   - k % 8 == 0 and n % 8 == 0 (row pitches must be multiples of 16 bytes
+ *     for the tensor-memory-access engine), m, n, k < 2^31
+ *     (GEMM_ERR_UNSUPPORTED_SHAPE).  There is no fallback kernel.
+ *   - the current device must be compute capability 10.3 (GEMM_ERR_ARCH).
+ *   - a launch failure reported by the CUDA runtime -> GEMM_ERR_LAUNCH.
+ *   - a pipeline wait inside the kernel that ran past its time limit is
+ *     recorded on the device and reported later by gemm_f16_take_device_error
+ *     as GEMM_ERR_TIMEOUT; the kernel returns instead of hanging.
+ */
+#ifndef GEMM_F16_H_
+#define GEMM_F16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,
+    GEMM_ERR_ALIGNMENT = 2,
+    GEMM_ERR_UNSUPPORTED_SHAPE = 3,
+    GEMM_ERR_ARCH = 4,
+    GEMM_ERR_WORKSPACE = 5,
+    GEMM_ERR_LAUNCH = 6,
+    GEMM_ERR_TIMEOUT = 7,
+    GEMM_ERR_CUDA = 8
+} gemm_status_t;
+
+/*
+ * A launch plan: sizes only, no pointers, no device handles.  Produced by
+ * the plan queries below, consumed by gemm_f16_nt_run.  All fields are plain
+ * integers so a caller can inspect (and, for measurement, adjust) them.
+ *
+ * Tile rasterization follows "4. Pipeline Abstraction and Two Consumer Warp
+ * Groups", section "Tile Rasterization": tile ids are walked in groups of
+ * `raster_width` N-columns, row-major inside a group, the last group being
+ * narrower when tiles_n is not a multiple of the width.
+ */
+typedef struct gemm_f16_plan {
+    int32_t variant;         /* compiled kernel instance, see gemm_f16_variant_info */
+    int32_t cta_group;       /* 1: one CTA per MMA tile; 2: a CTA pair (cluster of 2) shares one */
+    int32_t block_m;         /* output rows per MMA tile (128 * cta_group) */
+    int32_t block_n;         /* output columns per MMA tile */
+    int32_t block_k;         /* K depth of one pipeline stage (64) */
+    int32_t stages;          /* shared-memory ring depth */
+    int32_t raster_width;    /* N-columns per raster group (>= 1) */
+    int32_t split_k;         /* K partitions (1 = none) */
+    int64_t m, n, k;
+    int64_t tiles_m, tiles_n, num_tiles;
+    int64_t k_blocks;        /* ceil(k / block_k) */
+    int32_t grid;            /* CTAs launched (persistent: <= resident slots) */
+    int32_t cluster;         /* CTAs per cluster (= cta_group) */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t num_sms;         /* SM count the plan was made for */
+    uint64_t workspace_bytes;/* device workspace the plan needs (0 = none) */
+} gemm_f16_plan_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gemm_f16_status_string(gemm_status_t status);
+
+/* Number of compiled kernel variants, and the shape of one of them.
+ * Returns GEMM_ERR_INVALID_ARG for an index out of range. */
+int32_t gemm_f16_variant_count(void);
+gemm_status_t gemm_f16_variant_info(int32_t variant, int32_t *cta_group, int32_t *block_n,
+                                    int32_t *stages, int32_t *smem_bytes);
+
+/*
+ * Plan for the current CUDA device: validates the shape, checks the device
+ * is compute capability 10.3, picks a variant and the grid.  Host only,
+ * allocates nothing, launches nothing.
+ */
+gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t *out);
+
+/*
+ * Plan for a device with `num_sms` SMs (and `max_clusters` co-resident
+ * 2-CTA clusters, or 0 for num_sms / 2) without touching any device.
+ * `variant` < 0 picks automatically; `raster_width` <= 0 and `split_k`
+ * <= 0 pick automatically.  Pure host code: it is the planning logic the
+ * device entry points use, exposed for inspection and tests.
+ */
+gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_sms,
+                                   int32_t max_clusters, int32_t variant, int32_t raster_width,
+                                   int32_t split_k, gemm_f16_plan_t *out);
+
+/* Device workspace (bytes) gemm_f16_nt_ws needs for this shape on the
+ * current device; 0 when the chosen plan needs none. */
+gemm_status_t gemm_f16_nt_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes);
+
+/*
+ * C = A . B^T on `stream`.  a: device pointer to M*K fp16, b: device pointer
+ * to N*K fp16, c: device pointer to M*N fp16.  Plans automatically; if the
+ * chosen plan needs a workspace this entry point picks the best plan that
+ * needs none instead.
+ */
+gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
+                          void *c, gemm_stream_t stream);
+
+/* As gemm_f16_nt with a caller-owned device workspace of ws_bytes bytes
+ * (may be NULL/0 when the plan needs none; too small -> GEMM_ERR_WORKSPACE). */
+gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
+                             void *c, void *workspace, size_t ws_bytes, gemm_stream_t stream);
+
+/* Launch a given plan (from gemm_f16_nt_plan or gemm_f16_nt_plan_for, made
+ * for the current device's SM count).  The plan is re-validated. */
+gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c,
+                              void *workspace, size_t ws_bytes, gemm_stream_t stream);
+
+/*
+ * End-to-end form for host-resident data: copies a_host (M*K fp16) and
+ * b_host (N*K fp16) into the caller's device buffers a_dev / b_dev, runs
+ * the GEMM into c_dev, and copies c_dev back to c_host (M*N fp16), all
+ * enqueued on `stream` (asynchronous; pinned host memory makes the copies
+ * truly asynchronous).  Allocates nothing.
+ */
+gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_host,
+                               const void *b_host, void *c_host, void *a_dev, void *b_dev,
+                               void *c_dev, gemm_stream_t stream);
+
+/*
+ * Reads and clears the current device's error word after synchronizing
+ * `stream`.  Returns GEMM_ERR_TIMEOUT if a kernel since the last call gave
+ * up on a pipeline wait (*code, if non-NULL, receives which wait: see the
+ * source), GEMM_OK otherwise, GEMM_ERR_CUDA if the runtime fails.
+ */
+gemm_status_t gemm_f16_take_device_error(gemm_stream_t stream, uint32_t *code);
+
+/*
+ * Host evaluation of the scheduler's arithmetic, the same inline functions
+ * the kernel runs, for inspection and tests:
+ *   gemm_f16_raster_coord: tile id -> (m_block, n_block) for a tiles_m x
+ *     tiles_n grid walked in groups of `raster_width` N-columns.
+ *   gemm_f16_fast_divmod: quotient and remainder of n by d (d >= 1) by the
+ *     precomputed multiply-and-shift the kernel uses.
+ */
+gemm_status_t gemm_f16_raster_coord(int64_t tiles_m, int64_t tiles_n, int32_t raster_width,
+                                    int64_t tile, int64_t *m_block, int64_t *n_block);
+gemm_status_t gemm_f16_fast_divmod(uint32_t d, uint32_t n, uint32_t *q, uint32_t *r);
+
+/*
+ * Failure-detection hook for tests (no counterpart on the reference pages):
+ * launches `plan` like gemm_f16_nt_run, except that the TMA producer of CTA 0
+ * leaves its `skip_fill`-th ring-stage fill undone and every pipeline wait is
+ * limited to `wait_limit_cycles` SM clock cycles.  The starved waits then
+ * expire, the kernel records the failure in the device error word, frees its
+ * tensor memory and returns; gemm_f16_take_device_error reports
+ * GEMM_ERR_TIMEOUT.  C is left partly unwritten.  No fault, trap or hang.
+ */
+gemm_status_t gemm_f16_nt_run_stall_test(const gemm_f16_plan_t *plan, const void *a, const void *b,
+                                         void *c, uint32_t skip_fill, long long wait_limit_cycles,
+                                         gemm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H_ */

@@ -1,0 +1,54 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C
+ABI on numpy operands and compare with the CPU oracle."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from dense_fp16_gemm_03_gb300 import gemm as G  # noqa: E402
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    G.lib()
+
+
+def num_sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def to_dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.float16).to("cuda")
+
+
+def from_dev_bits(c):
+    return c.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def run_gpu(A, B, variant=None, raster_width=0, stream=None):
+    """C bits (uint16 [M,N]) from the CUDA path.  variant None = automatic plan."""
+    M, K = A.shape
+    N = B.shape[0]
+    a, b = to_dev(A), to_dev(B)
+    c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    if variant is None and raster_width == 0:
+        G.gemm_f16_nt(a, b, c, stream=stream)
+    else:
+        plan = G.gemm_f16_nt_plan_for(M, N, K, num_sms(), 0, -1 if variant is None else variant, raster_width, 0)
+        G.gemm_f16_nt_run(plan, a, b, c, stream=stream)
+    st, code = G.gemm_f16_take_device_error(stream)
+    assert st == G.GEMM_OK, "device error word 0x%x" % code
+    return from_dev_bits(c)
+
+
+def assert_parity(c_bits, A, B, exact=False):
+    ref, absum = oracle.gemm_nt(A, B)
+    if exact:
+        bad = np.argwhere(c_bits != ref)
+        assert bad.size == 0, "first mismatch at %s: gpu 0x%04x oracle 0x%04x (%d mismatches)" % (
+            tuple(bad[0]), c_bits[tuple(bad[0])], ref[tuple(bad[0])], len(bad))
+    rep = oracle.check_parity(c_bits, ref, absum, index_shape=ref.shape)
+    assert rep.ok, repr(rep)
+    return rep

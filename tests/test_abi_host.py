@@ -1,0 +1,153 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, exports
+every declared symbol, validates arguments before touching a device, plans
+deterministically, and its scheduler arithmetic (raster map, fast division)
+is exact.  The scheduler functions checked here are the same inline code
+the kernel runs."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from dense_fp16_gemm_03_gb300 import build as pkg_build
+from dense_fp16_gemm_03_gb300 import gemm as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    pkg_build.build()
+    return G.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "gemm_f16.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    assert len(names) >= 14
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(names) == set(G.EXPORTED)
+
+
+def test_status_strings(L):
+    for s in range(9):
+        assert G.status_string(s).startswith("GEMM_")
+    assert "unknown" in G.status_string(99)
+
+
+def test_variant_table(L):
+    n = G.gemm_f16_variant_count()
+    assert n >= 2
+    for v in range(n):
+        info = G.gemm_f16_variant_info(v)
+        assert info["cta_group"] in (1, 2)
+        assert info["block_n"] % 64 == 0
+        assert info["smem_bytes"] <= 232448
+    with pytest.raises(G.GemmError):
+        G.gemm_f16_variant_info(n)
+
+
+def test_fast_divmod_brute_force(L):
+    rng = np.random.Generator(np.random.PCG64(0))
+    divisors = list(range(1, 300)) + [int(x) for x in rng.integers(1, 2 ** 32, size=200)] + [
+        2 ** 31, 2 ** 31 + 1, 2 ** 32 - 1, 65535, 65536, 65537]
+    numerators = [0, 1, 2, 2 ** 31 - 1, 2 ** 31, 2 ** 32 - 1] + [int(x) for x in rng.integers(0, 2 ** 32, size=60)]
+    for d in divisors:
+        for n in numerators + [d - 1, d, d + 1, 2 * d - 1, (2 ** 32 - 1) // d * d]:
+            if not 0 <= n < 2 ** 32:
+                continue
+            q, r = G.gemm_f16_fast_divmod(d, n)
+            assert (q, r) == divmod(n, d), (d, n)
+    with pytest.raises(G.GemmError):
+        G.gemm_f16_fast_divmod(0, 5)
+
+
+def _reference_raster(tiles_m, tiles_n, width, t):
+    """Grouped raster, written out independently: groups of `width`
+    N-columns (the last one narrower), row-major (N fastest) inside."""
+    width = max(1, min(width, tiles_n))
+    group = t // (width * tiles_m)
+    n_first = group * width
+    w = min(width, tiles_n - n_first)
+    r = t - group * width * tiles_m
+    return r // w, n_first + r % w
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n", [(1, 1), (1, 64), (64, 1), (7, 5), (13, 29), (32, 32), (24, 20), (2, 2),
+                                             (64, 32), (3, 17)])
+@pytest.mark.parametrize("width", [1, 2, 3, 4, 8, 16, 100])
+def test_raster_is_a_bijection_and_grouped(L, tiles_m, tiles_n, width):
+    seen = set()
+    for t in range(tiles_m * tiles_n):
+        mb, nb = G.gemm_f16_raster_coord(tiles_m, tiles_n, width, t)
+        assert 0 <= mb < tiles_m and 0 <= nb < tiles_n
+        assert (mb, nb) == _reference_raster(tiles_m, tiles_n, width, t)
+        seen.add((mb, nb))
+    assert len(seen) == tiles_m * tiles_n
+
+
+def test_raster_width_one_is_plain_row_major(L):
+    for t in range(5 * 7):
+        # width 1: each group is one N-column, walked down M
+        assert G.gemm_f16_raster_coord(5, 7, 1, t) == (t % 5, t // 5)
+
+
+def test_plan_for_shapes(L):
+    p = G.gemm_f16_nt_plan_for(8192, 8192, 8192, 148)
+    assert p.block_k == 64 and p.k_blocks == 128
+    assert p.tiles_m * p.block_m >= 8192 and p.tiles_n * p.block_n >= 8192
+    assert p.num_tiles == p.tiles_m * p.tiles_n
+    assert p.grid % p.cluster == 0 and p.grid <= 148
+    assert p.workspace_bytes == 0
+    r = G.gemm_f16_nt_plan_for(3000, 5000, 4096, 148)
+    assert r.tiles_m == -(-3000 // r.block_m) and r.tiles_n == -(-5000 // r.block_n)
+    for v in range(G.gemm_f16_variant_count()):
+        q = G.gemm_f16_nt_plan_for(128, 16384, 16384, 148, variant=v, raster_width=4)
+        assert q.variant == v and q.raster_width == 4
+        assert q.grid // q.cluster <= q.num_tiles
+
+
+@pytest.mark.parametrize("m,n,k,status", [
+    (-1, 8, 8, G.GEMM_ERR_INVALID_ARG),
+    (8, 12, 8, G.GEMM_ERR_UNSUPPORTED_SHAPE),      # n % 8
+    (8, 8, 12, G.GEMM_ERR_UNSUPPORTED_SHAPE),      # k % 8
+    (2 ** 31, 8, 8, G.GEMM_ERR_UNSUPPORTED_SHAPE),
+])
+def test_plan_rejects_bad_shapes(L, m, n, k, status):
+    p = G.Plan()
+    assert L.gemm_f16_nt_plan_for(m, n, k, 148, 0, -1, 0, 0, ctypes.byref(p)) == status
+
+
+def test_argument_errors_before_any_device_call(L):
+    """Pointer and shape validation happens on the host before any CUDA call."""
+    good = 1 << 20
+    assert L.gemm_f16_nt(8, 8, 8, None, good, good, None) == G.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_nt(8, 8, 8, good, good, None, None) == G.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_nt(8, 8, 8, good + 2, good, good, None) == G.GEMM_ERR_ALIGNMENT
+    assert L.gemm_f16_nt(8, 8, 8, good, good + 8, good, None) == G.GEMM_ERR_ALIGNMENT
+    assert L.gemm_f16_nt(8, 8, 8, good, good, good + 4, None) == G.GEMM_ERR_ALIGNMENT
+    assert L.gemm_f16_nt(8, 12, 8, good, good, good, None) == G.GEMM_ERR_UNSUPPORTED_SHAPE
+    assert L.gemm_f16_nt(8, 8, 10, good, good, good, None) == G.GEMM_ERR_UNSUPPORTED_SHAPE
+    assert L.gemm_f16_nt(-3, 8, 8, good, good, good, None) == G.GEMM_ERR_INVALID_ARG
+    # empty output: a no-op that needs no pointers at all
+    assert L.gemm_f16_nt(0, 8, 8, None, None, None, None) == G.GEMM_OK
+    assert L.gemm_f16_nt(8, 0, 8, None, None, None, None) == G.GEMM_OK
+    assert L.gemm_f16_nt_run(None, good, good, good, None, 0, None) == G.GEMM_ERR_INVALID_ARG
+
+
+def test_no_cuda_device_is_an_error_not_a_crash(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    good = 1 << 20
+    st = L.gemm_f16_nt(128, 128, 64, good, good, good, None)
+    assert st == G.GEMM_ERR_CUDA
+    p = G.Plan()
+    assert L.gemm_f16_nt_plan(128, 128, 64, ctypes.byref(p)) == G.GEMM_ERR_CUDA

@@ -1,0 +1,193 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer-valued operands ({-8..8}/8) make every partial sum exact in fp32
+and in double, so the GPU must match the oracle bit for bit there; real-
+valued operands must meet |gpu - oracle| <= 1e-3 * sum|a*b| + ulp16(oracle)
+element by element.  Sizes span several tiles and ragged tails; the full
+workloads are checked at their real sizes (entirely, or on sampled entries
+the oracle computes one by one for the 8192^3 product).
+"""
+import numpy as np
+import pytest
+
+from gpu_helpers import assert_parity, from_dev_bits, num_sms, require_gpu, run_gpu, to_dev, torch
+
+import oracle
+from dense_fp16_gemm_03_gb300 import gemm as G
+from dense_fp16_gemm_03_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _variants():
+    return list(range(G.gemm_f16_variant_count()))
+
+
+# ------------------------------------------------------------------ small
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_square_256_exact_every_variant(variant):
+    w = inputs.BY_NAME["square_256"]
+    A, B = inputs.workload_operands(w)
+    c = run_gpu(A, B, variant=variant)
+    assert_parity(c, A, B, exact=True)
+
+
+def test_day78_lcg_operands_256():
+    A, B = inputs.lcg_eighths(256, 256, 256)
+    assert_parity(run_gpu(A, B), A, B, exact=True)
+
+
+RAGGED = [(1, 8, 8), (3, 8, 16), (129, 264, 72), (128, 256, 64), (257, 136, 200), (300, 520, 136),
+          (640, 1032, 520), (1000, 1000, 1000), (96, 2056, 264)]
+
+
+@pytest.mark.parametrize("shape", RAGGED)
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_ragged_exact(shape, variant):
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=M + 7 * N + 13 * K)
+    assert_parity(run_gpu(A, B, variant=variant), A, B, exact=True)
+
+
+@pytest.mark.parametrize("shape", [(129, 264, 72), (777, 1000, 1536), (1024, 1024, 4096)])
+@pytest.mark.parametrize("dist", ["normal", "uniform"])
+def test_real_valued_tolerance(shape, dist):
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, dist, seed=M * N + K)
+    for v in _variants():
+        assert_parity(run_gpu(A, B, variant=v), A, B)
+
+
+@pytest.mark.parametrize("width", [1, 2, 3, 5, 8, 64])
+def test_raster_width_does_not_change_results(width):
+    A, B = inputs.make_operands(700, 1800, 256, "eighths", seed=5)
+    ref = run_gpu(A, B, variant=0, raster_width=1)
+    for v in _variants():
+        assert np.array_equal(run_gpu(A, B, variant=v, raster_width=width), ref)
+
+
+# ------------------------------------------------------ structured operands
+
+@pytest.mark.parametrize("n", [128, 200, 256, 520])
+def test_identity_and_permutation(n):
+    rng = np.random.Generator(np.random.PCG64(n))
+    B = rng.standard_normal((n, n)).astype(np.float16)
+    for v in _variants():
+        c = run_gpu(inputs.identity(n), B, variant=v)          # = B^T exactly
+        assert np.array_equal(oracle.f16_to_f64(c), B.T.astype(np.float64))
+        P, p = inputs.permutation(n, seed=n + 1)
+        c = run_gpu(P, B, variant=v)                            # C[i, j] = B[j, p[i]]
+        assert np.array_equal(oracle.f16_to_f64(c), B[:, p].T.astype(np.float64))
+        c = run_gpu(B, inputs.identity(n), variant=v)          # = B exactly
+        assert np.array_equal(oracle.f16_to_f64(c), B.astype(np.float64))
+
+
+@pytest.mark.parametrize("shape", [(129, 264, 72), (256, 512, 640), (300, 8, 4096)])
+def test_rank1_closed_form(shape):
+    M, N, K = shape
+    A, B, (u, w, v) = inputs.rank1(M, N, K, seed=K)
+    expect = (np.outer(u, w) * float(np.sum(v * v))).astype(np.float16).view(np.uint16)
+    for var in _variants():
+        assert np.array_equal(run_gpu(A, B, variant=var), expect)
+
+
+# ----------------------------------------------------------------- edges
+
+def test_empty_and_zero_k():
+    a = torch.zeros((0, 64), dtype=torch.float16, device="cuda")
+    b = torch.zeros((16, 64), dtype=torch.float16, device="cuda")
+    c = torch.empty((0, 16), dtype=torch.float16, device="cuda")
+    G.gemm_f16_nt(a, b, c)
+    a = torch.randn((40, 0), device="cuda").half()
+    b = torch.randn((24, 0), device="cuda").half()
+    c = torch.full((40, 24), 7.0, dtype=torch.float16, device="cuda")
+    G.gemm_f16_nt(a, b, c)                                      # empty sum: C := 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c).item() == 0
+
+
+def test_guard_bands_untouched():
+    M, N, K = 300, 520, 136
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=9)
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), float("nan"), dtype=torch.float16, device="cuda")
+    c = buf[guard:guard + M * N].view(M, N)
+    G.gemm_f16_nt(to_dev(A), to_dev(B), c)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[guard + M * N:]).all()
+    assert_parity(from_dev_bits(c), A, B, exact=True)
+
+
+def test_misaligned_pointer_rejected_without_launch():
+    a = torch.zeros(64 * 64 + 8, dtype=torch.float16, device="cuda")
+    b = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    c = torch.full((64, 64), 3.0, dtype=torch.float16, device="cuda")
+    st = G.lib().gemm_f16_nt(64, 64, 64, a.data_ptr() + 2, b.data_ptr(), c.data_ptr(),
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == G.GEMM_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert (c == 3.0).all()
+
+
+def test_side_stream_and_host_entry_point():
+    M, N, K = 384, 640, 320
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=21)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = run_gpu(A, B, stream=s)
+    assert_parity(c, A, B, exact=True)
+    a_h = torch.from_numpy(A.view(np.int16)).view(torch.float16).pin_memory()
+    b_h = torch.from_numpy(B.view(np.int16)).view(torch.float16).pin_memory()
+    c_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    a_d = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    b_d = torch.empty((N, K), dtype=torch.float16, device="cuda")
+    c_d = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    G.gemm_f16_nt_host(a_h, b_h, c_h, a_d, b_d, c_d, stream=s)
+    s.synchronize()
+    assert_parity(c_h.view(torch.int16).numpy().view(np.uint16), A, B, exact=True)
+
+
+def test_plan_matches_device():
+    p = G.gemm_f16_nt_plan(8192, 8192, 8192)
+    assert p.num_sms == num_sms()
+    assert G.gemm_f16_nt_workspace_size(8192, 8192, 8192) == p.workspace_bytes == 0
+
+
+# ------------------------------------------------------- full workloads
+
+def _full(name):
+    w = inputs.BY_NAME[name]
+    A, B = inputs.workload_operands(w)
+    return w, A, B
+
+
+@pytest.mark.parametrize("name", ["square_256", "ragged_3000x5000x4096"])
+def test_integer_workloads_bit_exact(name):
+    w, A, B = _full(name)
+    assert_parity(run_gpu(A, B), A, B, exact=True)
+
+
+@pytest.mark.parametrize("name", ["square_4096", "skinny_128x16384x16384"])
+def test_real_workloads_full_tolerance(name):
+    w, A, B = _full(name)
+    assert_parity(run_gpu(A, B), A, B)
+
+
+def test_square_8192_sampled():
+    w, A, B = _full("square_8192")
+    c = run_gpu(A, B)
+    rng = np.random.Generator(np.random.PCG64(8192))
+    rows = np.concatenate([rng.integers(0, 8192, size=6000), np.arange(8192), np.full(2048, 8191),
+                           np.arange(128)])
+    cols = np.concatenate([rng.integers(0, 8192, size=6000), np.arange(8192)[::-1], np.arange(6144, 8192),
+                           np.full(128, 8191)])
+    ref, absum = oracle.gemm_nt_entries(A, B, rows, cols)
+    rep = oracle.check_parity(c[rows, cols], ref, absum)
+    assert rep.ok, repr(rep)
+    assert not np.isnan(oracle.f16_to_f64(c)).any()
