@@ -1,0 +1,383 @@
+"""Benchmark of the GB300 fp16 NT GEMM, C[M,N] = A[M,K] . B[N,K]^T.
+
+One step = one GEMM of the workload (default: M = N = K = 8192, operands
+uniform on [-1, 1) rounded to fp16, seed 1003) through the C ABI, with A, B
+and C resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+--impl reference times the CPU oracle (double accumulation, fp16 rounding)
+on this machine's host cores over a bounded sample of the same workload:
+the only reference that exists for this product is that definition.
+
+Multi-GPU (torchrun, one rank per GPU): each rank runs its own replica of
+the workload (the product needs no exchange); value = all ranks' flops /
+the slowest rank's time ("scaling": "weak").
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from dense_fp16_gemm_03_gb300 import inputs  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (2MNK/time) at 1 GB300; fraction of dense fp16 tensor peak"
+UNIT = "TFLOP/s"
+NOMINAL_PEAK_TFLOPS = 2250.0      # dense fp16/bf16 tensor peak quoted for GB300
+FALLBACK_PEAK_TFLOPS = 1700.0     # bf16 sustained, measured earlier on a GB300
+L2_BYTES = 129 * 10 ** 6
+KERNEL_SOURCES = ["dense_fp16_gemm_03_gb300/csrc/gemm_kernel.cuh", "dense_fp16_gemm_03_gb300/csrc/ptx.cuh",
+                  "dense_fp16_gemm_03_gb300/csrc/sched.cuh", "dense_fp16_gemm_03_gb300/csrc/gemm_api.cu"]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def traffic_record(workload_name, plan):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources with the same plan; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    entry = rec.get("workloads", {}).get(workload_name)
+    if entry is None:
+        return None
+    if any(getattr(plan, k) != v for k, v in entry.get("plan", {}).items()):
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [s for (t, s) in self.samples if self.t0 is not None and self.t0 - 0.05 <= t <= self.t1 + 0.15]
+        use = inside if inside else [s for (_, s) in self.samples]
+        if not use:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[2]) for s in use if len(s) > 2 and num(s[2]) is not None]
+        smax = [num(s[3]) for s in use if len(s) > 3 and num(s[3]) is not None]
+        power = [num(s[4]) for s in use if len(s) > 4 and num(s[4]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in use for i in range(4) if len(s) > 6 + i and s[6 + i].lower() == "active"})
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "reasons": reasons,
+            "samples": len(use),
+            "samples_in_timed_region": len(inside),
+        }
+
+
+def cpu_oracle_rate(A, B, target_s=10.0):
+    """Time the CPU oracle on the first R rows of C (all N columns, full K),
+    R sized for about target_s seconds and at least one row per oracle
+    thread.  Returns (tflops, seconds, rows)."""
+    import oracle
+
+    M, K = A.shape
+    N = B.shape[0]
+    rows = min(M, max(1, oracle.num_threads()))
+    while True:
+        t = time.perf_counter()
+        oracle.gemm_nt(A[:rows], B)
+        dt = time.perf_counter() - t
+        if dt > min(0.5, target_s / 4) or rows >= M:
+            break
+        rows = min(M, rows * 4)
+    want = max(min(M, oracle.num_threads()), min(M, int(rows * target_s / max(dt, 1e-6))))
+    if want != rows:
+        rows = want
+        t = time.perf_counter()
+        oracle.gemm_nt(A[:rows], B)
+        dt = time.perf_counter() - t
+    return 2.0 * rows * N * K / dt / 1e12, dt, rows
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+
+    A, B = inputs.workload_operands(w)
+    threads = oracle.num_threads()
+    # each step is a bounded sample of the workload: the first R rows of C
+    _, probe_s, rows = cpu_oracle_rate(A, B, target_s=min(10.0, max(0.05, 120.0 / (args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        oracle.gemm_nt(A[:rows], B)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_nt(A[:rows], B)
+    dt = (time.perf_counter() - t) / max(1, args.steps)
+    value = 2.0 * rows * w.N * w.K / dt / 1e12
+    sample = "first %d of %d rows of C (all %d columns, full K=%d) per step" % (rows, w.M, w.N, w.K)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {
+        "workload": "%s: C[%d,%d] = A[%d,%d] . B[%d,%d]^T fp16, %s operands, seed %d" % (
+            w.name, w.M, w.N, w.M, w.K, w.N, w.K, w.dist, w.seed),
+        "M": w.M, "N": w.N, "K": w.K, "distribution": w.dist, "seed": w.seed,
+        "l2": ("inputs larger than L2: %.0f MiB of A, B and C per step vs %d MB L2" % (
+            w.algorithmic_bytes / 2 ** 20, L2_BYTES // 10 ** 6)) if w.algorithmic_bytes > L2_BYTES
+        else "working set smaller than L2 (no flush)",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="square_8192", choices=sorted(inputs.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--variant", type=int, default=-1, help="force a compiled kernel variant (measurement)")
+    ap.add_argument("--raster", type=int, default=0, help="force a raster width (measurement)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = inputs.BY_NAME[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    import torch
+    from dense_fp16_gemm_03_gb300 import gemm as G
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    G.lib()
+    dev = torch.device("cuda", local)
+    A, B = inputs.workload_operands(w)
+    a = torch.from_numpy(A.view(np.int16)).view(torch.float16).to(dev)
+    b = torch.from_numpy(B.view(np.int16)).view(torch.float16).to(dev)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    if args.variant >= 0 or args.raster > 0:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        plan = G.gemm_f16_nt_plan_for(w.M, w.N, w.K, sms, 0, args.variant, args.raster, 0)
+        step = lambda: G.gemm_f16_nt_run(plan, a, b, c, stream=stream)  # noqa: E731
+    else:
+        plan = G.gemm_f16_nt_plan(w.M, w.N, w.K)
+        step = lambda: G.gemm_f16_nt(a, b, c, stream=stream)  # noqa: E731
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    st, code = G.gemm_f16_take_device_error(stream)
+    if st != G.GEMM_OK:
+        raise RuntimeError("kernel reported error word 0x%x" % code)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark_begin()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark_end()
+    clocks = sampler.stop()
+    st, code = G.gemm_f16_take_device_error(stream)
+    if st != G.GEMM_OK:
+        raise RuntimeError("kernel reported error word 0x%x" % code)
+    total_ms = starts[0].elapsed_time(ends[-1])
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the host-buffer entry point: H2D of A and B from
+    # pinned memory, the GEMM, D2H of C, every step
+    e2e = None
+    if not args.no_e2e:
+        a_h = torch.from_numpy(A.view(np.int16)).view(torch.float16).pin_memory()
+        b_h = torch.from_numpy(B.view(np.int16)).view(torch.float16).pin_memory()
+        c_h = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+        e_steps = max(3, min(args.steps, 200))
+        for _ in range(3):
+            G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, stream=stream)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(e_steps):
+            G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * w.flops * e_steps / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * (w.M * w.K + w.N * w.K), "d2h_bytes_per_step": 2 * w.M * w.N,
+               "steps": e_steps}
+
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    # The timed loop runs the kernel back to back for a long stretch under
+    # the board power cap, so the comparable denominator is the sustained
+    # (back-to-back, power-capped) cuBLAS bf16 figure; fp16 and bf16 have the
+    # same nominal tensor rate.  The burst figure is reported beside it.
+    burst = None
+    if peaks and "bf16_tflops_sustained" in peaks:
+        peak = float(peaks["bf16_tflops_sustained"])
+        peak_note = "of measured: cuBLAS bf16 sustained (back to back under the power cap); fp16 rate = bf16 rate"
+        burst = float(peaks.get("bf16_tflops", 0.0)) or None
+    else:
+        peak, peak_note = FALLBACK_PEAK_TFLOPS, "of fallback"
+    achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+        "peak_source": peak_note, "traffic": traffic_record(w.name, plan),
+        "algorithmic_bytes": w.algorithmic_bytes, "kernel": "gemm_f16_nt_kernel",
+        "frac_of_nominal_2250": achieved / NOMINAL_PEAK_TFLOPS,
+        "burst_peak": burst, "frac_of_burst": (achieved / burst) if burst else None,
+    }
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        rate, secs, rows = cpu_oracle_rate(A, B, target_s=10.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": "first %d of %d rows of C (all %d columns, full K=%d), %.1f s" % (rows, w.M, w.N, w.K, secs)}
+    cfg = workload_config(w)
+    cfg["plan"] = {k: v for k, v in plan.as_dict().items() if k in (
+        "variant", "cta_group", "block_m", "block_n", "stages", "raster_width", "grid")}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
+        "frac_of_nominal_peak": value / world / NOMINAL_PEAK_TFLOPS,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -178,42 +178,25 @@ int64_t cdiv(int64_t a, int64_t b)
 
 // --------------------------------------------------------------- plans
 
-// Raster width: enough N-columns per group that a wave of concurrently
-// running tiles forms a roughly square block of the tile grid.
-int32_t auto_raster_width(int64_t tiles_m, int64_t tiles_n, int64_t slots)
+// Raster width: N-columns per raster group.  Measured on GB300 (8192^3,
+// 256 x 256 pair tiles, interleaved runs under the power cap): widths 8-16
+// kept the clock highest (fewest DRAM re-reads) and gave the best
+// throughput; 1-4 re-read A from DRAM more often.
+int32_t auto_raster_width(int64_t tiles_n)
 {
-    int64_t w = 1;
-    while (w * w < slots && w < tiles_n) w *= 2;
+    int64_t w = 8;
     if (w > tiles_n) w = tiles_n;
-    (void)tiles_m;
     return int32_t(w < 1 ? 1 : w);
 }
 
-// Tile-shape choice: among the compiled variants, minimise the number of
-// full waves of tiles over the resident CTA slots, weighted by the work of
-// one tile; ties go to the larger tile (less operand traffic per flop).
-int32_t auto_variant(int64_t m, int64_t n, int32_t num_sms, int32_t max_clusters)
+// Tile-shape choice, from measurement on GB300: the 256 x 256 CTA-pair
+// tile (variant 2) is fastest on every shape with more than 128 rows; a
+// single 128-row tile (M <= 128) leaves the second CTA of a pair idle, and
+// there the one-CTA 128 x 128 tile (variant 1) is fastest.
+int32_t auto_variant(int64_t m, int64_t n)
 {
-    int best = 0;
-    double best_cost = 0.0;
-    for (int v = 0; v < kNumVariants; ++v) {
-        const Variant &var = kVariants[v];
-        const int64_t bm = 128 * var.cg;
-        const int64_t tiles = cdiv(m, bm) * cdiv(n, var.bn);
-        int64_t slots = (var.cg == 2) ? (max_clusters > 0 ? max_clusters : num_sms / 2) : num_sms;
-        if (slots < 1) slots = 1;
-        const int64_t waves = cdiv(tiles, slots);
-        // time ~ waves x (tile work / per-slot throughput); a pair has twice the tensor cores
-        const double tile_work = double(bm) * double(var.bn) / double(var.cg);
-        // larger tiles re-read less: small penalty per unit of operand traffic per flop
-        const double traffic = 1.0 / double(bm) + 1.0 / double(var.bn);
-        const double cost = double(waves) * tile_work * (1.0 + 8.0 * traffic);
-        if (v == 0 || cost < best_cost * 0.999) {
-            best = v;
-            best_cost = cost;
-        }
-    }
-    return best;
+    (void)n;
+    return m <= 128 ? 1 : 2;
 }
 
 gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters_in,
@@ -226,7 +209,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     if (variant >= kNumVariants) return GEMM_ERR_INVALID_ARG;
     if (split_k > 1) return GEMM_ERR_INVALID_ARG;  // no split-K kernel in this build
     const int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / 2;
-    if (variant < 0) variant = auto_variant(m, n, num_sms, max_clusters);
+    if (variant < 0) variant = auto_variant(m, n);
     const Variant &var = kVariants[variant];
     gemm_f16_plan_t p;
     memset(&p, 0, sizeof(p));
@@ -252,7 +235,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     if (slots < 1) slots = 1;
     const int64_t clusters = p.num_tiles < slots ? p.num_tiles : slots;
     p.grid = int32_t(clusters * var.cg);
-    if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_m, p.tiles_n, slots);
+    if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_n);
     if (p.tiles_n > 0 && raster_width > p.tiles_n) raster_width = int32_t(p.tiles_n);
     if (raster_width < 1) raster_width = 1;
     p.raster_width = raster_width;
@@ -417,7 +400,7 @@ gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t 
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
-    const int32_t auto_v = auto_variant(m, n, dev->num_sms, dev->max_clusters[2]);
+    const int32_t auto_v = auto_variant(m, n);
     return make_plan(m, n, k, dev->num_sms, dev->max_clusters[auto_v], auto_v, 0, 1, out);
 }
 
