@@ -231,6 +231,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--variant", type=int, default=-1, help="force a compiled kernel variant (measurement)")
     ap.add_argument("--raster", type=int, default=0, help="force a raster width (measurement)")
+    ap.add_argument("--stream-k", type=int, default=-1, help="force stream-K off (0) or on (1) (measurement)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -254,13 +255,16 @@ def main():
     b = torch.from_numpy(B.view(np.int16)).view(torch.float16).to(dev)
     c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    if args.variant >= 0 or args.raster > 0:
+    if args.variant >= 0 or args.raster > 0 or args.stream_k >= 0:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        plan = G.gemm_f16_nt_plan_for(w.M, w.N, w.K, sms, 0, args.variant, args.raster, 0)
-        step = lambda: G.gemm_f16_nt_run(plan, a, b, c, stream=stream)  # noqa: E731
+        plan = G.gemm_f16_nt_plan_ex(w.M, w.N, w.K, args.variant, args.raster, args.stream_k)
+        ws = G.workspace_for(plan, dev)
+        step = lambda: G.gemm_f16_nt_run(plan, a, b, c, ws, stream=stream)  # noqa: E731
     else:
+        # the automatic plan through the workspace entry point (stream-K tail when it pays)
         plan = G.gemm_f16_nt_plan(w.M, w.N, w.K)
-        step = lambda: G.gemm_f16_nt(a, b, c, stream=stream)  # noqa: E731
+        ws = G.workspace_for(plan, dev)
+        step = lambda: G.gemm_f16_nt_ws(a, b, c, ws, stream=stream)  # noqa: E731
 
     for _ in range(args.warmup):
         step()
@@ -310,7 +314,7 @@ def main():
         c_h = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
         e_steps = max(3, min(args.steps, 200))
         for _ in range(3):
-            G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, stream=stream)
+            G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, ws, stream=stream)
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if dist is not None:
@@ -318,7 +322,7 @@ def main():
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(e_steps):
-            G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, stream=stream)
+            G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, ws, stream=stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1)
@@ -364,7 +368,8 @@ def main():
                "sample": "first %d of %d rows of C (all %d columns, full K=%d), %.1f s" % (rows, w.M, w.N, w.K, secs)}
     cfg = workload_config(w)
     cfg["plan"] = {k: v for k, v in plan.as_dict().items() if k in (
-        "variant", "cta_group", "block_m", "block_n", "stages", "raster_width", "grid")}
+        "variant", "cta_group", "block_m", "block_n", "stages", "raster_width", "grid", "stream_k", "dp_tiles",
+        "workspace_bytes")}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

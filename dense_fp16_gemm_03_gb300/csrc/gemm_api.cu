@@ -30,46 +30,47 @@ constexpr int kMaxDevices = 64;
 // ------------------------------------------------------------ variants
 
 struct Variant {
-    int cg, bn, stages, smem;
+    int cg, bn, stages, mc, smem;
     const void *fn;
     cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
 };
 
-template <int CG, int BN, int ST>
+template <int CG, int BN, int ST, int MC>
 cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(unsigned(plan.grid), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST>::kSmemBytes);
+    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC>::kSmemBytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     int na = 0;
-    if (CG == 2) {
+    if (CG * MC > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = CG * MC;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         na = 1;
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST>, params);
+    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC>, params);
 }
 
-#define GEMM_VARIANT(CG, BN, ST)                                                                 \
-    Variant                                                                                      \
-    {                                                                                            \
-        CG, BN, ST, KernelCfg<CG, BN, ST>::kSmemBytes,                                           \
-            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST>), &launch_variant<CG, BN, ST> \
+#define GEMM_VARIANT(CG, BN, ST, MC)                                                                     \
+    Variant                                                                                              \
+    {                                                                                                    \
+        CG, BN, ST, MC, KernelCfg<CG, BN, ST, MC>::kSmemBytes,                                           \
+            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC>), &launch_variant<CG, BN, ST, MC> \
     }
 
 const Variant kVariants[] = {
-    GEMM_VARIANT(1, 256, 4),  // 0: 128 x 256 tile, one CTA
-    GEMM_VARIANT(1, 128, 6),  // 1: 128 x 128 tile, one CTA
-    GEMM_VARIANT(2, 256, 6),  // 2: 256 x 256 tile on a CTA pair
-    GEMM_VARIANT(2, 128, 8),  // 3: 256 x 128 tile on a CTA pair
+    GEMM_VARIANT(1, 256, 4, 1),  // 0: 128 x 256 tile, one CTA
+    GEMM_VARIANT(1, 128, 6, 1),  // 1: 128 x 128 tile, one CTA
+    GEMM_VARIANT(2, 256, 6, 1),  // 2: 256 x 256 tile on a CTA pair
+    GEMM_VARIANT(2, 128, 8, 1),  // 3: 256 x 128 tile on a CTA pair
+    GEMM_VARIANT(2, 256, 6, 2),  // 4: two pairs stacked along M share B by multicast (512 x 256 per cluster)
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -114,16 +115,17 @@ gemm_status_t device_info(DeviceInfo **out)
                     return GEMM_ERR_CUDA;
                 }
                 d.attr_set[v] = true;
-                d.max_clusters[v] = sms / var.cg;
-                if (var.cg == 2) {
+                const int cs = var.cg * var.mc;
+                d.max_clusters[v] = sms / cs;
+                if (cs > 1) {
                     cudaLaunchConfig_t cfg;
                     memset(&cfg, 0, sizeof(cfg));
-                    cfg.gridDim = dim3(unsigned(2 * (sms / 2)), 1, 1);
+                    cfg.gridDim = dim3(unsigned(cs * (sms / cs)), 1, 1);
                     cfg.blockDim = dim3(kNumThreads, 1, 1);
                     cfg.dynamicSmemBytes = size_t(var.smem);
                     cudaLaunchAttribute attr;
                     attr.id = cudaLaunchAttributeClusterDimension;
-                    attr.val.clusterDim.x = 2;
+                    attr.val.clusterDim.x = unsigned(cs);
                     attr.val.clusterDim.y = 1;
                     attr.val.clusterDim.z = 1;
                     cfg.attrs = &attr;
@@ -199,27 +201,51 @@ int32_t auto_variant(int64_t m, int64_t n)
     return m <= 128 ? 1 : 2;
 }
 
+int64_t round_up(int64_t x, int64_t a)
+{
+    return (x + a - 1) / a * a;
+}
+
+// Stream-K workspace: one fp32 partial tile per CTA, then one flag per CTA.
+int64_t streamk_partials_bytes(int64_t grid, int32_t block_n)
+{
+    return round_up(grid * 128 * int64_t(block_n) * 4, 256);
+}
+
+int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
+{
+    return streamk_partials_bytes(grid, block_n) + round_up(grid * 4, 256);
+}
+
+// A stream-K tail pays when the data-parallel schedule would leave a last
+// wave of tiles noticeably short of the resident clusters.
+bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
+{
+    if (k_blocks < 4 || num_tiles * k_blocks < 2 * slots) return false;
+    const int64_t waves = cdiv(num_tiles, slots);
+    return double(num_tiles) / double(waves * slots) < 0.98;
+}
+
 gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters_in,
-                        int32_t variant, int32_t raster_width, int32_t split_k, gemm_f16_plan_t *out)
+                        int32_t variant, int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_shape(m, n, k);
     if (st != GEMM_OK) return st;
     if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
-    if (variant >= kNumVariants) return GEMM_ERR_INVALID_ARG;
-    if (split_k > 1) return GEMM_ERR_INVALID_ARG;  // no split-K kernel in this build
-    const int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / 2;
+    if (variant >= kNumVariants || stream_k > 1) return GEMM_ERR_INVALID_ARG;
     if (variant < 0) variant = auto_variant(m, n);
     const Variant &var = kVariants[variant];
+    const int32_t cs = var.cg * var.mc;  // CTAs per cluster
+    const int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / cs;
     gemm_f16_plan_t p;
     memset(&p, 0, sizeof(p));
     p.variant = variant;
     p.cta_group = var.cg;
-    p.block_m = 128 * var.cg;
+    p.block_m = 128 * cs;
     p.block_n = var.bn;
     p.block_k = kBlockK;
     p.stages = var.stages;
-    p.split_k = 1;
     p.m = m;
     p.n = n;
     p.k = k;
@@ -227,19 +253,36 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.tiles_n = cdiv(n, p.block_n);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = cdiv(k, kBlockK);
-    p.cluster = var.cg;
+    p.cluster = cs;
     p.smem_bytes = var.smem;
     p.num_sms = num_sms;
-    p.workspace_bytes = 0;
-    int64_t slots = (var.cg == 2) ? max_clusters : num_sms;
+    if (p.num_tiles >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    int64_t slots = (cs > 1) ? max_clusters : num_sms;
     if (slots < 1) slots = 1;
-    const int64_t clusters = p.num_tiles < slots ? p.num_tiles : slots;
-    p.grid = int32_t(clusters * var.cg);
+    int64_t clusters = p.num_tiles < slots ? p.num_tiles : slots;
+    p.stream_k = 0;
+    p.dp_tiles = p.num_tiles;
+    p.sk_iters = 0;
+    p.workspace_bytes = 0;
+    const bool want_sk = stream_k == 1 || (stream_k < 0 && streamk_pays(p.num_tiles, p.k_blocks, slots));
+    if (want_sk && p.num_tiles > 0) {
+        // whole waves but the last one or two stay data-parallel; the rest is split evenly
+        const int64_t full_waves = p.num_tiles / slots;
+        const int64_t dp = full_waves >= 1 ? (full_waves - 1) * slots : 0;
+        const int64_t sk_iters = (p.num_tiles - dp) * p.k_blocks;
+        if (sk_iters >= slots) {
+            clusters = slots;
+            p.stream_k = 1;
+            p.dp_tiles = dp;
+            p.sk_iters = sk_iters;
+            p.workspace_bytes = uint64_t(streamk_workspace_bytes(clusters * cs, var.bn));
+        }
+    }
+    p.grid = int32_t(clusters * cs);
     if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_n);
     if (p.tiles_n > 0 && raster_width > p.tiles_n) raster_width = int32_t(p.tiles_n);
     if (raster_width < 1) raster_width = 1;
     p.raster_width = raster_width;
-    if (p.num_tiles >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED_SHAPE;
     *out = p;
     return GEMM_OK;
 }
@@ -299,15 +342,28 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         }
         return GEMM_OK;
     }
-    // the plan must be one this library would make: re-derive and compare
+    // the plan must be consistent with what this library computes for its shape
     gemm_f16_plan_t check;
-    st = make_plan(plan.m, plan.n, plan.k, plan.num_sms, 0, plan.variant, plan.raster_width, plan.split_k, &check);
+    st = make_plan(plan.m, plan.n, plan.k, plan.num_sms, 0, plan.variant, plan.raster_width, 0, &check);
     if (st != GEMM_OK) return st;
-    // (any grid of whole clusters is correct: the kernel walks the tiles persistently)
     if (check.variant != plan.variant || check.tiles_m != plan.tiles_m || check.tiles_n != plan.tiles_n ||
         check.k_blocks != plan.k_blocks || check.smem_bytes != plan.smem_bytes || plan.cluster != check.cluster ||
-        plan.grid < plan.cluster || plan.grid % plan.cluster != 0 || plan.grid / plan.cluster > plan.num_tiles)
+        plan.grid < plan.cluster || plan.grid % plan.cluster != 0)
         return GEMM_ERR_INVALID_ARG;
+    const int64_t workers = plan.grid / plan.cluster;
+    if (plan.stream_k == 0) {
+        // any grid of whole clusters is correct: the kernel walks the tiles persistently
+        if (plan.dp_tiles != plan.num_tiles || plan.sk_iters != 0 || workers > plan.num_tiles)
+            return GEMM_ERR_INVALID_ARG;
+    } else {
+        // owners wait for contributors: every cluster must be resident at once
+        if (plan.stream_k != 1 || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
+            plan.sk_iters != (plan.num_tiles - plan.dp_tiles) * plan.k_blocks || plan.sk_iters < workers ||
+            workers > dev->max_clusters[plan.variant] ||
+            int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, plan.block_n))
+            return GEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
+    }
     const Variant &var = kVariants[plan.variant];
 
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -318,7 +374,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     st = encode_matrix(enc, &params.tmap_a, a, uint64_t(plan.m), uint64_t(plan.k), kBlockK, 128);
     if (st != GEMM_OK) return st;
     st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.n), uint64_t(plan.k), kBlockK,
-                       uint32_t(var.bn / var.cg));
+                       uint32_t(var.bn / var.cg / var.mc));
     if (st != GEMM_OK) return st;
     st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
     if (st != GEMM_OK) return st;
@@ -328,6 +384,17 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     params.k = uint32_t(plan.k);
     params.num_tiles = uint32_t(plan.num_tiles);
     params.k_blocks = uint32_t(plan.k_blocks);
+    params.dp_tiles = uint32_t(plan.dp_tiles);
+    params.sk_iters = uint64_t(plan.sk_iters);
+    if (plan.stream_k) {
+        params.partials = static_cast<float *>(ws);
+        params.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) +
+                                                    streamk_partials_bytes(plan.grid, plan.block_n));
+        if (cudaMemsetAsync(params.flags, 0, size_t(plan.grid) * 4u, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
     params.skip_fill = skip_fill;
     params.wait_limit = wait_limit;
     void *err_ptr = nullptr;
@@ -387,28 +454,50 @@ gemm_status_t gemm_f16_variant_info(int32_t v, int32_t *cta_group, int32_t *bloc
 }
 
 gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters,
-                                   int32_t variant, int32_t raster_width, int32_t split_k, gemm_f16_plan_t *out)
+                                   int32_t variant, int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out)
 {
-    return make_plan(m, n, k, num_sms, max_clusters, variant, raster_width, split_k, out);
+    return make_plan(m, n, k, num_sms, max_clusters, variant, raster_width, stream_k, out);
 }
 
-gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t *out)
+}  // extern "C"
+
+namespace {
+
+// Plan for the current device; arguments as in gemm_f16_nt_plan_for.
+gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int32_t raster_width, int32_t stream_k,
+                          gemm_f16_plan_t *out)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_shape(m, n, k);
     if (st != GEMM_OK) return st;
+    if (variant >= kNumVariants) return GEMM_ERR_INVALID_ARG;
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
-    const int32_t auto_v = auto_variant(m, n);
-    return make_plan(m, n, k, dev->num_sms, dev->max_clusters[auto_v], auto_v, 0, 1, out);
+    const int32_t v = variant < 0 ? auto_variant(m, n) : variant;
+    return make_plan(m, n, k, dev->num_sms, dev->max_clusters[v], v, raster_width, stream_k, out);
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t *out)
+{
+    return device_plan(m, n, k, -1, 0, -1, out);
+}
+
+gemm_status_t gemm_f16_nt_plan_ex(int64_t m, int64_t n, int64_t k, int32_t variant, int32_t raster_width,
+                                  int32_t stream_k, gemm_f16_plan_t *out)
+{
+    return device_plan(m, n, k, variant, raster_width, stream_k, out);
 }
 
 gemm_status_t gemm_f16_nt_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes)
 {
     if (!bytes) return GEMM_ERR_INVALID_ARG;
     gemm_f16_plan_t p;
-    gemm_status_t st = gemm_f16_nt_plan(m, n, k, &p);
+    gemm_status_t st = device_plan(m, n, k, -1, 0, -1, &p);
     if (st != GEMM_OK) return st;
     *bytes = size_t(p.workspace_bytes);
     return GEMM_OK;
@@ -423,7 +512,7 @@ gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, con
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
     gemm_f16_plan_t p;
-    st = gemm_f16_nt_plan(m, n, k, &p);
+    st = device_plan(m, n, k, -1, 0, -1, &p);
     if (st != GEMM_OK) return st;
     return run_plan(p, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
                     default_wait_limit(p.k_blocks));
@@ -432,7 +521,16 @@ gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, con
 gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *c,
                           gemm_stream_t stream)
 {
-    return gemm_f16_nt_ws(m, n, k, a, b, c, nullptr, 0, stream);
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    st = check_pointers(m, n, k, a, b, c);
+    if (st != GEMM_OK) return st;
+    if (m == 0 || n == 0) return GEMM_OK;
+    gemm_f16_plan_t p;
+    st = device_plan(m, n, k, -1, 0, 0, &p);
+    if (st != GEMM_OK) return st;
+    return run_plan(p, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                    default_wait_limit(p.k_blocks));
 }
 
 gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c, void *workspace,
@@ -456,7 +554,8 @@ gemm_status_t gemm_f16_nt_run_stall_test(const gemm_f16_plan_t *plan, const void
 }
 
 gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_host, const void *b_host,
-                               void *c_host, void *a_dev, void *b_dev, void *c_dev, gemm_stream_t stream)
+                               void *c_host, void *a_dev, void *b_dev, void *c_dev, void *workspace,
+                               size_t ws_bytes, gemm_stream_t stream)
 {
     gemm_status_t st = check_shape(m, n, k);
     if (st != GEMM_OK) return st;
@@ -472,7 +571,8 @@ gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_ho
             return GEMM_ERR_CUDA;
         }
     }
-    st = gemm_f16_nt(m, n, k, a_dev, b_dev, c_dev, stream);
+    st = workspace ? gemm_f16_nt_ws(m, n, k, a_dev, b_dev, c_dev, workspace, ws_bytes, stream)
+                   : gemm_f16_nt(m, n, k, a_dev, b_dev, c_dev, stream);
     if (st != GEMM_OK) return st;
     if (cudaMemcpyAsync(c_host, c_dev, size_t(m) * size_t(n) * 2u, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
         cudaGetLastError();

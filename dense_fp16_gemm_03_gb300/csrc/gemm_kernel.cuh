@@ -27,6 +27,23 @@
 // CTA of the pair issues the MMA for both, and each CTA's tensor memory
 // holds its own 128 output rows.
 //
+// MC > 1 (with CG == 2) stacks MC CTA pairs along M in one cluster: the
+// pairs work on vertically adjacent tiles that need the same B columns, so
+// each CTA loads only 1/MC of its half of the B tile and multicasts it to
+// the CTAs with the same rank-in-pair of the other pairs; a ring stage is
+// refilled only after every pair's MMAs have released it.  This cuts each
+// CTA's L2-to-shared traffic from A + B/2 to A + B/(2 MC) per K block.
+//
+// Stream-K tail (optional): the first dp_tiles tiles (whole waves) are
+// walked data-parallel, one tile per cluster at a time; the K iterations of
+// the remaining tiles are cut into equal contiguous ranges, one per cluster,
+// so the last wave is not partly idle.  A cluster whose range starts inside
+// a tile publishes its fp32 partial tile to the caller's workspace and sets
+// a flag; the cluster that holds the tile's first K block adds the
+// published partials in its epilogue.  That owning segment is the last one
+// in its range while the publishing segments are the first ones in theirs,
+// so no cluster ever waits on a cluster that waits on it.
+//
 // Ragged edges: loads outside [0,M)x[0,K) / [0,N)x[0,K) are zero-filled by
 // the TMA unit (so a partial K block adds zeros), stores outside [0,M)x[0,N)
 // are dropped by it, and store boxes that start outside C are skipped.
@@ -61,6 +78,7 @@ enum : uint32_t {
     kErrWaitAccEmpty = 3,
     kErrWaitAccFull = 4,
     kErrWaitDrain = 5,
+    kErrWaitPartial = 6,
 };
 
 struct KernelParams {
@@ -71,18 +89,26 @@ struct KernelParams {
     uint32_t m, n, k;
     uint32_t num_tiles;
     uint32_t k_blocks;
+    uint32_t dp_tiles;    // tiles [0, dp_tiles) are walked data-parallel
+    uint64_t sk_iters;    // K iterations of tiles [dp_tiles, num_tiles), split evenly over the clusters
+    float *partials;      // stream-K workspace: one 128 x BN fp32 partial tile per CTA
+    uint32_t *flags;      // stream-K workspace: one "partial published" flag per CTA, zero at launch
     uint32_t skip_fill;   // test hook: k-block fill (counted across CTA 0's tiles) the producer
                           // of CTA 0 leaves undone, to exercise the bounded waits; ~0u = none
     long long wait_limit; // cycles a single barrier wait may take before it gives up
     uint32_t *error_word;
 };
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, int MC = 1>
 struct KernelCfg {
     static_assert(CG == 1 || CG == 2, "cta group");
+    static_assert(MC == 1 || (CG == 2 && (MC == 2 || MC == 4)), "B multicast needs CTA pairs");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N");
-    static constexpr int kBM = 128 * CG;            // MMA M
-    static constexpr int kBNCta = BN / CG;          // B rows loaded per CTA
+    static constexpr int kCS = CG * MC;             // CTAs per cluster
+    static constexpr int kBM = 128 * CG;            // MMA M (one pair)
+    static constexpr int kBMCluster = kBM * MC;     // output rows per scheduling unit
+    static constexpr int kBNCta = BN / CG;          // B rows in one CTA's ring stage
+    static constexpr int kBSlice = kBNCta / MC;     // B rows one CTA loads per stage
     static constexpr int kABytes = 128 * kBlockK * 2;
     static constexpr int kBBytes = kBNCta * kBlockK * 2;
     static constexpr int kStageTx = (kABytes + kBBytes) * CG;  // bytes landing on one full barrier
@@ -96,7 +122,7 @@ struct KernelCfg {
     static constexpr int kSmemUsed = kOffAbort + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
-    static_assert(kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
+    static_assert(kBBytes % 1024 == 0 && kABytes % 1024 == 0 && (kBSlice * 128) % 1024 == 0, "swizzle atoms");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
 
@@ -145,16 +171,44 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     }
 }
 
+// First stream-K iteration of cluster w (of `workers`).
+__device__ __forceinline__ uint64_t sk_begin(const KernelParams &p, uint32_t w, uint32_t workers)
+{
+    return uint64_t(w) * p.sk_iters / workers;
+}
+
+// Every role walks the same sequence of segments (tile, [k_lo, k_hi)):
+// data-parallel tiles first, then this cluster's stream-K range.  f returns
+// false to stop early (abort).
+template <class F>
+__device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t worker, uint32_t workers, F &&f)
+{
+    for (uint32_t tile = worker; tile < p.dp_tiles; tile += workers)
+        if (!f(tile, 0u, p.k_blocks)) return;
+    if (p.sk_iters == 0) return;
+    uint64_t it = sk_begin(p, worker, workers);
+    const uint64_t end = sk_begin(p, worker + 1, workers);
+    while (it < end) {
+        const uint64_t u = it / p.k_blocks;
+        const uint32_t k_lo = uint32_t(it - u * p.k_blocks);
+        const uint64_t left = end - it;
+        const uint32_t k_hi = (left >= uint64_t(p.k_blocks - k_lo)) ? p.k_blocks : k_lo + uint32_t(left);
+        if (!f(p.dp_tiles + uint32_t(u), k_lo, k_hi)) return;
+        it += k_hi - k_lo;
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits)
 {
     __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int CG, int BN, int STAGES>
+template <int CG, int BN, int STAGES, int MC>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = KernelCfg<CG, BN, STAGES>;
+    using Cfg = KernelCfg<CG, BN, STAGES, MC>;
+    constexpr int CS = Cfg::kCS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -162,10 +216,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t cta_rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
-    const bool leader = (cta_rank == 0);
-    const uint32_t cluster_id = blockIdx.x / CG;
-    const uint32_t num_clusters = gridDim.x / CG;
+    const uint32_t cta_rank = (CS > 1) ? ptx::cluster_ctarank() : 0u;  // rank in the cluster
+    const uint32_t pair_rank = (CG == 2) ? (cta_rank & 1u) : 0u;        // rank in the CTA pair
+    const uint32_t pair = cta_rank / CG;                                  // pair index in the cluster
+    const uint32_t pair_leader = cta_rank - pair_rank;                    // cluster rank of the pair's first CTA
+    const bool leader = (pair_rank == 0);
+    const uint32_t cluster_id = blockIdx.x / CS;
+    const uint32_t num_clusters = gridDim.x / CS;
+    // CTAs whose B slices land in this CTA's stage: same rank-in-pair, every pair
+    uint16_t same_rank_mask = 0;
+#pragma unroll
+    for (int q = 0; q < MC; ++q) same_rank_mask |= uint16_t(1u << (q * CG + pair_rank));
 
     auto bar_full = [&](uint32_t s) { return base + Cfg::kOffBar + 8u * s; };
     auto bar_empty = [&](uint32_t s) { return base + Cfg::kOffBar + 8u * (STAGES + s); };
@@ -178,7 +239,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full(s), 1);
-            ptx::mbar_init(bar_empty(s), 1);
+            ptx::mbar_init(bar_empty(s), MC);  // released by the MMA issuer of every pair
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_acc_full(b), 1);
@@ -196,7 +257,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before_sync();
-    if constexpr (CG == 2) ptx::cluster_sync();
+    if constexpr (CS > 1) ptx::cluster_sync();
     else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
@@ -204,19 +265,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol_a = ptx::policy_evict_normal();
-            const uint64_t pol_b = ptx::policy_evict_normal();
             uint32_t stage = 0, phase = 0, fills = 0;
             bool ok = true;
-            for (uint32_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+            for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
                 uint32_t mb, nb;
                 raster_coord(p.raster, tile, mb, nb);
-                const int32_t m0 = int32_t(mb * Cfg::kBM + cta_rank * 128u);
-                const int32_t n0 = int32_t(nb * BN + cta_rank * Cfg::kBNCta);
-                for (uint32_t kb = 0; kb < p.k_blocks; ++kb, ++fills) {
+                const int32_t m0 = int32_t(mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u);
+                const int32_t n0 = int32_t(nb * BN + pair_rank * Cfg::kBNCta + pair * Cfg::kBSlice);
+                for (uint32_t kb = k_lo; kb < k_hi; ++kb, ++fills) {
                     if (!wait_bounded<CG>(bar_empty(stage), phase ^ 1u, p, abort_flag, kErrWaitEmpty)) {
                         ok = false;
-                        break;
+                        return false;
                     }
                     const bool skip = (blockIdx.x == 0) && (fills == p.skip_fill);
                     if (!skip) {
@@ -226,13 +285,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                         const int32_t k0 = int32_t(kb * kBlockK);
                         if constexpr (CG == 1) {
                             ptx::mbar_arrive_expect_tx(fb, Cfg::kStageTx);
-                            ptx::tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0, pol_a);
-                            ptx::tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0, pol_b);
+                            ptx::tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
+                            ptx::tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
                         } else {
-                            const uint32_t fb_leader = ptx::map_to_rank(fb, 0);
+                            const uint32_t fb_leader = ptx::map_to_rank(fb, pair_leader);
                             if (leader) ptx::mbar_arrive_expect_tx(fb, Cfg::kStageTx);
-                            ptx::tma_load_2d_pair(a_dst, &p.tmap_a, fb_leader, k0, m0, pol_a);
-                            ptx::tma_load_2d_pair(b_dst, &p.tmap_b, fb_leader, k0, n0, pol_b);
+                            ptx::tma_load_2d_pair(a_dst, &p.tmap_a, fb_leader, k0, m0);
+                            if constexpr (MC == 1)
+                                ptx::tma_load_2d_pair(b_dst, &p.tmap_b, fb_leader, k0, n0);
+                            else
+                                ptx::tma_load_2d_pair_mc(b_dst + pair * Cfg::kBSlice * 128u, &p.tmap_b, fb_leader, k0,
+                                                         n0, same_rank_mask);
                         }
                     }
                     if (++stage == STAGES) {
@@ -240,7 +303,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                         phase ^= 1u;
                     }
                 }
-            }
+                return true;
+            });
             if (!ok) __nanosleep(100000);  // let copies already issued land before teardown
         }
     } else if (warp == 1) {
@@ -248,19 +312,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         if (leader && lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(Cfg::kBM, BN);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool ok = true;
-            for (uint32_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
-                if (!wait_bounded<CG>(bar_acc_empty(acc), acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty)) {
-                    ok = false;
-                    break;
-                }
+            for_each_segment(p, cluster_id, num_clusters, [&](uint32_t, uint32_t k_lo, uint32_t k_hi) {
+                if (!wait_bounded<CG>(bar_acc_empty(acc), acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty))
+                    return false;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (uint32_t kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!wait_bounded<CG>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) {
-                        ok = false;
-                        break;
-                    }
+                for (uint32_t kb = k_lo; kb < k_hi; ++kb) {
+                    if (!wait_bounded<CG>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
                     ptx::tc_fence_after_sync();
                     const uint64_t a_desc = smem_desc_sw128(base + Cfg::kOffA + stage * Cfg::kABytes);
                     const uint64_t b_desc = smem_desc_sw128(base + Cfg::kOffB + stage * Cfg::kBBytes);
@@ -268,26 +326,27 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         // +32 bytes along K inside the swizzle atom per 16-element step
                         ptx::mma_f16<CG>(d_tmem, a_desc + uint64_t(2 * kk), b_desc + uint64_t(2 * kk), idesc,
-                                         (kb | uint32_t(kk)) != 0u);
+                                         (kb != k_lo || kk != 0) ? 1u : 0u);
                     }
+                    // the stage is free in every CTA whose producer writes into this pair's stage
                     if constexpr (CG == 1) ptx::mma_commit(bar_empty(stage));
-                    else ptx::mma_commit_pair(bar_empty(stage), uint16_t(0x3));
+                    else ptx::mma_commit_pair(bar_empty(stage), uint16_t((1u << CS) - 1u));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (!ok) break;
                 if constexpr (CG == 1) ptx::mma_commit(bar_acc_full(acc));
-                else ptx::mma_commit_pair(bar_acc_full(acc), uint16_t(0x3));
+                else ptx::mma_commit_pair(bar_acc_full(acc), uint16_t(0x3u << pair_leader));
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
-            }
+                return true;
+            });
             // No MMA may still be running when the tensor memory is freed.
             if constexpr (CG == 1) ptx::mma_commit(bar_drain);
-            else ptx::mma_commit_pair(bar_drain, uint16_t(0x1));
+            else ptx::mma_commit_pair(bar_drain, uint16_t(1u << cta_rank));
             const long long t0 = clock64();
             while (!ptx::mbar_try_wait(bar_drain, 0)) {
                 if (clock64() - t0 > p.wait_limit) {
@@ -301,62 +360,132 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         const uint32_t quarter = warp & 3u;  // tensor-memory lanes [32q, 32q + 32) belong to this warp
         const uint32_t stage_base = base + Cfg::kOffStore + (warp - 2u) * 2u * kStoreBufBytes;
         const uint32_t lane_sel = (quarter * 32u) << 16;
+        constexpr uint32_t kSlotFloats = 128u * BN;          // one CTA's partial tile
+        constexpr uint32_t kChunkFloats = 32u * kStoreCols;  // one warp's 32 x 64 piece
+        const bool first_epi_thread = (threadIdx.x == 64u);
         uint32_t acc = 0, acc_phase = 0, stores = 0;
-        for (uint32_t tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+        for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
-            const uint32_t row0 = mb * Cfg::kBM + cta_rank * 128u + quarter * 32u;
+            const uint32_t row0 = mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u + quarter * 32u;
             const uint32_t col0 = nb * BN;
             const bool ok = wait_bounded<CG>(bar_acc_full(acc), acc_phase, p, abort_flag, kErrWaitAccFull);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            // A split tile meets the other epilogue warps at named barrier 1 below, so the decision
+            // to stop must be the same in all four warps; a whole tile needs it per warp only.
+            const bool split = (k_lo != 0) || (k_hi != p.k_blocks);
+            const bool all_ok = split ? ptx::named_barrier_and(1, 32 * kEpiWarps, ok) : __all_sync(0xffffffffu, ok);
+            if (!all_ok) return false;
             ptx::tc_fence_after_sync();
-            if (row0 < p.m) {
+            const uint32_t acc_col = tmem_base + acc * BN + lane_sel;
+            // Partial-tile layout in the workspace: per warp quarter and 64-column chunk, 16 float4
+            // slots x 32 lanes, so every warp-wide 16-byte access is one contiguous 512-byte run.
+            const uint32_t piece = quarter * 32u * BN + lane * 4u;
+            if (k_lo != 0) {
+                // ---- publish this partial tile; the owner of the tile adds it
+                float *slot = p.partials + size_t(blockIdx.x) * kSlotFloats + piece;
+                if (row0 < p.m) {
 #pragma unroll 1
-                for (int c = 0; c < BN / kStoreCols; ++c) {
-                    const uint32_t col = col0 + uint32_t(c * kStoreCols);
-                    if (col >= p.n) break;
-                    uint32_t r[64];
-                    ptx::tmem_ld_32x32b_x64_wait(tmem_base + acc * BN + uint32_t(c * kStoreCols) + lane_sel, r);
-                    const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // this buffer's previous store has read it
-                    __syncwarp();
-                    const uint32_t row_addr = buf + lane * 128u;
+                    for (int c = 0; c < BN / kStoreCols; ++c) {
+                        if (col0 + uint32_t(c * kStoreCols) >= p.n) break;
+                        uint32_t r[64];
+                        ptx::tmem_ld_32x32b_x64_wait(acc_col + uint32_t(c * kStoreCols), r);
+                        float *dst = slot + c * kChunkFloats;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t w0 = pack_half2(r[8 * j + 0], r[8 * j + 1]);
-                        const uint32_t w1 = pack_half2(r[8 * j + 2], r[8 * j + 3]);
-                        const uint32_t w2 = pack_half2(r[8 * j + 4], r[8 * j + 5]);
-                        const uint32_t w3 = pack_half2(r[8 * j + 6], r[8 * j + 7]);
-                        // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r mod 8)
-                        ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), w0, w1, w2, w3);
+                        for (int j = 0; j < 16; ++j)
+                            ptx::st_global_cg_f4(dst + j * 128, __uint_as_float(r[4 * j]),
+                                                 __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                                                 __uint_as_float(r[4 * j + 3]));
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(&p.tmap_c, buf, int32_t(col), int32_t(row0));
-                        ptx::bulk_commit_group();
+                }
+                __threadfence();
+                ptx::named_barrier_sync(1, 32 * kEpiWarps);
+                if (first_epi_thread) ptx::st_release_gpu(p.flags + blockIdx.x, 1u);
+            } else {
+                // ---- a whole tile, or the owning segment of a split tile
+                uint32_t first_w = 0, last_w = 0;  // contributors [first_w, last_w)
+                if (k_hi != p.k_blocks) {
+                    const uint64_t tile_end = uint64_t(tile - p.dp_tiles + 1) * p.k_blocks;
+                    first_w = cluster_id + 1;
+                    last_w = first_w;
+                    while (last_w < num_clusters && sk_begin(p, last_w, num_clusters) < tile_end) ++last_w;
+                    if (first_epi_thread) {
+                        for (uint32_t w = first_w; w < last_w; ++w) {
+                            if (sk_begin(p, w, num_clusters) >= sk_begin(p, w + 1, num_clusters)) continue;
+                            const uint32_t *flag = p.flags + w * CS + cta_rank;
+                            const long long t0 = clock64();
+                            while (ptx::ld_acquire_gpu(flag) == 0u) {
+                                if (*abort_flag || clock64() - t0 > p.wait_limit) {
+                                    *abort_flag = 1u;
+                                    atomicCAS(p.error_word, 0u, kErrWaitPartial | (blockIdx.x << 8));
+                                    break;
+                                }
+                            }
+                        }
                     }
-                    ++stores;
+                    ptx::named_barrier_sync(1, 32 * kEpiWarps);
+                }
+                if (row0 < p.m) {
+#pragma unroll 1
+                    for (int c = 0; c < BN / kStoreCols; ++c) {
+                        const uint32_t col = col0 + uint32_t(c * kStoreCols);
+                        if (col >= p.n) break;
+                        uint32_t r[64];
+                        ptx::tmem_ld_32x32b_x64_wait(acc_col + uint32_t(c * kStoreCols), r);
+                        for (uint32_t w = first_w; w < last_w; ++w) {
+                            if (sk_begin(p, w, num_clusters) >= sk_begin(p, w + 1, num_clusters)) continue;
+                            const float *src =
+                                p.partials + size_t(w * CS + cta_rank) * kSlotFloats + piece + c * kChunkFloats;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float4 v = ptx::ld_global_cg_f4(src + j * 128);
+                                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                            }
+                        }
+                        const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
+                        if (lane == 0) ptx::bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                        __syncwarp();
+                        const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t w0 = pack_half2(r[8 * j + 0], r[8 * j + 1]);
+                            const uint32_t w1 = pack_half2(r[8 * j + 2], r[8 * j + 3]);
+                            const uint32_t w2 = pack_half2(r[8 * j + 4], r[8 * j + 5]);
+                            const uint32_t w3 = pack_half2(r[8 * j + 6], r[8 * j + 7]);
+                            // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r mod 8)
+                            ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), w0, w1, w2, w3);
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&p.tmap_c, buf, int32_t(col), int32_t(row0));
+                            ptx::bulk_commit_group();
+                        }
+                        ++stores;
+                    }
                 }
             }
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
                 if constexpr (CG == 1) ptx::mbar_arrive(bar_acc_empty(acc));
-                else ptx::mbar_arrive_cluster(ptx::map_to_rank(bar_acc_empty(acc), 0));
+                else ptx::mbar_arrive_cluster(ptx::map_to_rank(bar_acc_empty(acc), pair_leader));
             }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
-        }
+            return true;
+        });
         if (lane == 0) ptx::bulk_wait_group<0>();
     }
 
     // ---------------------------------------------------- teardown
     __syncwarp();
     ptx::tc_fence_before_sync();
-    if constexpr (CG == 2) ptx::cluster_sync();
+    if constexpr (CS > 1) ptx::cluster_sync();
     else __syncthreads();
     ptx::tc_fence_after_sync();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);

@@ -40,7 +40,7 @@ class Plan(ctypes.Structure):
         ("block_k", ctypes.c_int32),
         ("stages", ctypes.c_int32),
         ("raster_width", ctypes.c_int32),
-        ("split_k", ctypes.c_int32),
+        ("stream_k", ctypes.c_int32),
         ("m", ctypes.c_int64),
         ("n", ctypes.c_int64),
         ("k", ctypes.c_int64),
@@ -48,6 +48,8 @@ class Plan(ctypes.Structure):
         ("tiles_n", ctypes.c_int64),
         ("num_tiles", ctypes.c_int64),
         ("k_blocks", ctypes.c_int64),
+        ("dp_tiles", ctypes.c_int64),
+        ("sk_iters", ctypes.c_int64),
         ("grid", ctypes.c_int32),
         ("cluster", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32),
@@ -65,7 +67,7 @@ class Plan(ctypes.Structure):
 # every symbol the public header declares
 EXPORTED = [
     "gemm_f16_status_string", "gemm_f16_variant_count", "gemm_f16_variant_info",
-    "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_workspace_size",
+    "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_plan_ex", "gemm_f16_nt_workspace_size",
     "gemm_f16_nt", "gemm_f16_nt_ws", "gemm_f16_nt_run", "gemm_f16_nt_host",
     "gemm_f16_take_device_error", "gemm_f16_raster_coord", "gemm_f16_fast_divmod",
     "gemm_f16_nt_run_stall_test",
@@ -91,11 +93,12 @@ def lib():
         "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32]),
         "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),
         "gemm_f16_nt_plan_for": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, P]),
+        "gemm_f16_nt_plan_ex": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, P]),
         "gemm_f16_nt_workspace_size": (ctypes.c_int, [i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]),
         "gemm_f16_nt": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp]),
         "gemm_f16_nt_ws": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
         "gemm_f16_nt_run": (ctypes.c_int, [P, vp, vp, vp, vp, ctypes.c_size_t, vp]),
-        "gemm_f16_nt_host": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp]),
+        "gemm_f16_nt_host": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]),
         "gemm_f16_take_device_error": (ctypes.c_int, [vp, pu32]),
         "gemm_f16_raster_coord": (ctypes.c_int, [i64, i64, i32, i64, pi64, pi64]),
         "gemm_f16_fast_divmod": (ctypes.c_int, [u32, u32, pu32, pu32]),
@@ -154,11 +157,28 @@ def gemm_f16_nt_plan(m, n, k):
     return p
 
 
-def gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters=0, variant=-1, raster_width=0, split_k=0):
+def gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters=0, variant=-1, raster_width=0, stream_k=-1):
+    """stream_k: -1 automatic, 0 data-parallel only, 1 stream-K tail."""
     p = Plan()
-    _check(lib().gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters, variant, raster_width, split_k,
+    _check(lib().gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters, variant, raster_width, stream_k,
                                       ctypes.byref(p)), "gemm_f16_nt_plan_for")
     return p
+
+
+def gemm_f16_nt_plan_ex(m, n, k, variant=-1, raster_width=0, stream_k=-1):
+    """Plan for the current device with optional overrides (negative/zero = automatic)."""
+    p = Plan()
+    _check(lib().gemm_f16_nt_plan_ex(m, n, k, variant, raster_width, stream_k, ctypes.byref(p)),
+           "gemm_f16_nt_plan_ex")
+    return p
+
+
+def workspace_for(plan, device="cuda"):
+    """A torch uint8 buffer of the plan's workspace size (None if it needs none)."""
+    if plan.workspace_bytes == 0:
+        return None
+    import torch
+    return torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=device)
 
 
 def gemm_f16_nt_workspace_size(m, n, k):
@@ -206,12 +226,13 @@ def gemm_f16_nt_run(plan, a, b, c, workspace=None, stream=None):
     return c
 
 
-def gemm_f16_nt_host(a_host, b_host, c_host, a_dev, b_dev, c_dev, stream=None):
+def gemm_f16_nt_host(a_host, b_host, c_host, a_dev, b_dev, c_dev, workspace=None, stream=None):
     """End-to-end call on host tensors (pinned for asynchronous copies)."""
     m, k = a_host.shape
     n = b_host.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().gemm_f16_nt_host(m, n, k, _ptr(a_host), _ptr(b_host), _ptr(c_host), _ptr(a_dev), _ptr(b_dev),
-                                  _ptr(c_dev), _stream(stream)), "gemm_f16_nt_host")
+                                  _ptr(c_dev), _ptr(workspace), ws_bytes, _stream(stream)), "gemm_f16_nt_host")
     return c_host
 
 

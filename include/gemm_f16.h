@@ -79,16 +79,31 @@ typedef struct gemm_f16_plan {
     int32_t block_k;         /* K depth of one pipeline stage (64) */
     int32_t stages;          /* shared-memory ring depth */
     int32_t raster_width;    /* N-columns per raster group (>= 1) */
-    int32_t split_k;         /* K partitions (1 = none) */
+    int32_t stream_k;        /* 0: every tile data-parallel; 1: data-parallel waves + stream-K tail */
     int64_t m, n, k;
     int64_t tiles_m, tiles_n, num_tiles;
     int64_t k_blocks;        /* ceil(k / block_k) */
+    int64_t dp_tiles;        /* tiles walked data-parallel (all of them when stream_k == 0) */
+    int64_t sk_iters;        /* K-block iterations of the remaining tiles, split evenly over the clusters */
     int32_t grid;            /* CTAs launched (persistent: <= resident slots) */
     int32_t cluster;         /* CTAs per cluster (= cta_group) */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t num_sms;         /* SM count the plan was made for */
     uint64_t workspace_bytes;/* device workspace the plan needs (0 = none) */
 } gemm_f16_plan_t;
+
+/*
+ * Stream-K ("stream_k == 1"): the last one to two waves of tiles are not
+ * given one tile per cluster; their K-block iterations are cut into equal
+ * contiguous ranges, one per cluster, so no cluster idles in a partial last
+ * wave.  A tile split between clusters is finished by the cluster holding
+ * its first K block, which adds the fp32 partial tiles the others publish in
+ * the workspace.  Workspace layout: grid * block_m/cta_group * block_n fp32
+ * partial tiles, then grid 32-bit flags (cleared by the library before each
+ * launch).  Every cluster of the grid must be resident at once; the plan's
+ * grid never exceeds that.  The fp32 partial sums change the rounding order
+ * of split tiles only within the fp32 accumulation error.
+ */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *gemm_f16_status_string(gemm_status_t status);
@@ -101,37 +116,50 @@ gemm_status_t gemm_f16_variant_info(int32_t variant, int32_t *cta_group, int32_t
 
 /*
  * Plan for the current CUDA device: validates the shape, checks the device
- * is compute capability 10.3, picks a variant and the grid.  Host only,
- * allocates nothing, launches nothing.
+ * is compute capability 10.3, picks a variant, the grid and whether a
+ * stream-K tail pays (then workspace_bytes > 0).  Host only, allocates
+ * nothing, launches nothing.
  */
 gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t *out);
 
 /*
  * Plan for a device with `num_sms` SMs (and `max_clusters` co-resident
  * 2-CTA clusters, or 0 for num_sms / 2) without touching any device.
- * `variant` < 0 picks automatically; `raster_width` <= 0 and `split_k`
- * <= 0 pick automatically.  Pure host code: it is the planning logic the
+ * `variant` < 0 picks automatically; `raster_width` <= 0 picks
+ * automatically; `stream_k` < 0 picks automatically, 0 forbids and 1
+ * requests the stream-K tail.  Pure host code: it is the planning logic the
  * device entry points use, exposed for inspection and tests.
  */
 gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_sms,
                                    int32_t max_clusters, int32_t variant, int32_t raster_width,
-                                   int32_t split_k, gemm_f16_plan_t *out);
+                                   int32_t stream_k, gemm_f16_plan_t *out);
+
+/*
+ * As gemm_f16_nt_plan, with the choices of gemm_f16_nt_plan_for overridable
+ * (variant / raster_width / stream_k; negative or zero = automatic as
+ * there), using the current device's SM count and co-resident cluster count.
+ */
+gemm_status_t gemm_f16_nt_plan_ex(int64_t m, int64_t n, int64_t k, int32_t variant,
+                                  int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out);
 
 /* Device workspace (bytes) gemm_f16_nt_ws needs for this shape on the
- * current device; 0 when the chosen plan needs none. */
+ * current device (the stream-K partial tiles and flags); 0 when the chosen
+ * plan needs none. */
 gemm_status_t gemm_f16_nt_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes);
 
 /*
  * C = A . B^T on `stream`.  a: device pointer to M*K fp16, b: device pointer
- * to N*K fp16, c: device pointer to M*N fp16.  Plans automatically; if the
- * chosen plan needs a workspace this entry point picks the best plan that
- * needs none instead.
+ * to N*K fp16, c: device pointer to M*N fp16.  Plans automatically among the
+ * plans that need no workspace (no stream-K tail).
  */
 gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
                           void *c, gemm_stream_t stream);
 
-/* As gemm_f16_nt with a caller-owned device workspace of ws_bytes bytes
- * (may be NULL/0 when the plan needs none; too small -> GEMM_ERR_WORKSPACE). */
+/* As gemm_f16_nt with a caller-owned device workspace of ws_bytes bytes,
+ * 256-byte aligned: uses the automatic plan, with a stream-K tail when it
+ * pays.  workspace may be NULL/0 when gemm_f16_nt_workspace_size reports 0;
+ * too small -> GEMM_ERR_WORKSPACE, misaligned -> GEMM_ERR_ALIGNMENT.  Calls
+ * that share one workspace must not overlap on the GPU. */
 gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
                              void *c, void *workspace, size_t ws_bytes, gemm_stream_t stream);
 
@@ -143,13 +171,14 @@ gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const 
 /*
  * End-to-end form for host-resident data: copies a_host (M*K fp16) and
  * b_host (N*K fp16) into the caller's device buffers a_dev / b_dev, runs
- * the GEMM into c_dev, and copies c_dev back to c_host (M*N fp16), all
- * enqueued on `stream` (asynchronous; pinned host memory makes the copies
- * truly asynchronous).  Allocates nothing.
+ * the GEMM into c_dev (as gemm_f16_nt_ws with the given workspace, which
+ * may be NULL/0), and copies c_dev back to c_host (M*N fp16), all enqueued
+ * on `stream` (asynchronous; pinned host memory makes the copies truly
+ * asynchronous).  Allocates nothing.
  */
 gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_host,
                                const void *b_host, void *c_host, void *a_dev, void *b_dev,
-                               void *c_dev, gemm_stream_t stream);
+                               void *c_dev, void *workspace, size_t ws_bytes, gemm_stream_t stream);
 
 /*
  * Reads and clears the current device's error word after synchronizing

@@ -100,16 +100,16 @@ def test_raster_width_one_is_plain_row_major(L):
 
 
 def test_plan_for_shapes(L):
-    p = G.gemm_f16_nt_plan_for(8192, 8192, 8192, 148)
+    p = G.gemm_f16_nt_plan_for(8192, 8192, 8192, 148, stream_k=0)
     assert p.block_k == 64 and p.k_blocks == 128
     assert p.tiles_m * p.block_m >= 8192 and p.tiles_n * p.block_n >= 8192
     assert p.num_tiles == p.tiles_m * p.tiles_n
     assert p.grid % p.cluster == 0 and p.grid <= 148
     assert p.workspace_bytes == 0
-    r = G.gemm_f16_nt_plan_for(3000, 5000, 4096, 148)
+    r = G.gemm_f16_nt_plan_for(3000, 5000, 4096, 148, stream_k=0)
     assert r.tiles_m == -(-3000 // r.block_m) and r.tiles_n == -(-5000 // r.block_n)
     for v in range(G.gemm_f16_variant_count()):
-        q = G.gemm_f16_nt_plan_for(128, 16384, 16384, 148, variant=v, raster_width=4)
+        q = G.gemm_f16_nt_plan_for(128, 16384, 16384, 148, variant=v, raster_width=4, stream_k=0)
         assert q.variant == v and q.raster_width == 4
         assert q.grid // q.cluster <= q.num_tiles
 
@@ -151,3 +151,65 @@ def test_no_cuda_device_is_an_error_not_a_crash(L):
     assert st == G.GEMM_ERR_CUDA
     p = G.Plan()
     assert L.gemm_f16_nt_plan(128, 128, 64, ctypes.byref(p)) == G.GEMM_ERR_CUDA
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (8192, 8192, 8192),
+                                   (1000, 1000, 1000), (128, 256, 8192)])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+def test_stream_k_plan_invariants(L, shape, variant):
+    m, n, k = shape
+    for sms in (148, 152):
+        p = G.gemm_f16_nt_plan_for(m, n, k, sms, 0, variant, 0, 1)
+        workers = p.grid // p.cluster
+        if p.stream_k:
+            assert p.sk_iters == (p.num_tiles - p.dp_tiles) * p.k_blocks
+            assert p.sk_iters >= workers and p.dp_tiles % workers == 0
+            assert p.num_tiles - p.dp_tiles <= 2 * workers            # at most two waves are split
+            assert p.workspace_bytes >= p.grid * 128 * p.block_n * 4 + p.grid * 4
+            assert workers == sms // p.cluster
+        else:                                                         # too little work to split
+            assert p.workspace_bytes == 0 and p.dp_tiles == p.num_tiles and p.num_tiles * p.k_blocks < workers + sms
+        q = G.gemm_f16_nt_plan_for(m, n, k, sms, 0, variant, 0, 0)
+        assert q.stream_k == 0 and q.workspace_bytes == 0 and q.dp_tiles == q.num_tiles
+
+
+def _segments(p):
+    """The kernel's segment walk for every cluster, written out independently."""
+    workers = p.grid // p.cluster
+    out = {}
+    for w in range(workers):
+        segs = [(t, 0, p.k_blocks) for t in range(w, p.dp_tiles, workers)]
+        b, e = w * p.sk_iters // workers, (w + 1) * p.sk_iters // workers
+        it = b
+        while it < e:
+            u, lo = divmod(it, p.k_blocks)
+            hi = min(p.k_blocks, lo + (e - it))
+            segs.append((p.dp_tiles + u, lo, hi))
+            it += hi - lo
+        out[w] = segs
+    return out
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (128, 256, 8192)])
+def test_stream_k_covers_every_k_block_once(L, shape):
+    m, n, k = shape
+    for variant in range(G.gemm_f16_variant_count()):
+        p = G.gemm_f16_nt_plan_for(m, n, k, 152, 0, variant, 0, 1)
+        if not p.stream_k:
+            continue
+        cover = {}
+        owners = {}
+        for w, segs in _segments(p).items():
+            n_dp = sum(1 for (t, _, _) in segs if t < p.dp_tiles)
+            for i, (t, lo, hi) in enumerate(segs):
+                for kb in range(lo, hi):
+                    assert (t, kb) not in cover
+                    cover[(t, kb)] = w
+                if lo == 0 and hi < p.k_blocks:
+                    owners[t] = w
+                    assert i == len(segs) - 1                         # an owning segment ends its range
+                if lo > 0:
+                    assert i == n_dp                                  # a publishing segment starts the stream-K range
+        assert len(cover) == p.num_tiles * p.k_blocks
+        for t, w in owners.items():                                   # contributors come after the owner
+            assert all(cover[(t, kb)] >= w for kb in range(p.k_blocks))

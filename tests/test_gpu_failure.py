@@ -27,7 +27,7 @@ def test_starved_wait_reports_timeout_and_recovers(variant):
     A, B = inputs.make_operands(M, N, K, "eighths", seed=77)
     a, b = to_dev(A), to_dev(B)
     c = torch.zeros((M, N), dtype=torch.float16, device="cuda")
-    plan = G.gemm_f16_nt_plan_for(M, N, K, num_sms(), 0, variant, 0, 0)
+    plan = G.gemm_f16_nt_plan_ex(M, N, K, variant, 0, 0)
     assert G.gemm_f16_take_device_error()[0] == G.GEMM_OK
     st = G.gemm_f16_nt_run_stall_test(plan, a, b, c, 3, WAIT_LIMIT_CYCLES)
     assert st == G.GEMM_OK                       # the launch itself is fine

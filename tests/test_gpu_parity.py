@@ -30,7 +30,7 @@ def _variants():
 
 # ------------------------------------------------------------------ small
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_square_256_exact_every_variant(variant):
     w = inputs.BY_NAME["square_256"]
     A, B = inputs.workload_operands(w)
@@ -48,7 +48,7 @@ RAGGED = [(1, 8, 8), (3, 8, 16), (129, 264, 72), (128, 256, 64), (257, 136, 200)
 
 
 @pytest.mark.parametrize("shape", RAGGED)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
 def test_ragged_exact(shape, variant):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "eighths", seed=M + 7 * N + 13 * K)
@@ -70,6 +70,52 @@ def test_raster_width_does_not_change_results(width):
     ref = run_gpu(A, B, variant=0, raster_width=1)
     for v in _variants():
         assert np.array_equal(run_gpu(A, B, variant=v, raster_width=width), ref)
+
+
+# -------------------------------------------------------------- stream-K
+
+SK_SHAPES = [(640, 1032, 520), (1000, 1000, 1000), (300, 520, 4096), (128, 256, 8192), (2304, 2304, 1024),
+             (129, 264, 72), (3000, 5000, 512)]
+
+
+@pytest.mark.parametrize("shape", SK_SHAPES)
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+def test_stream_k_exact(shape, variant):
+    """Split tiles are summed from fp32 partials; on integer-valued operands
+    every partial and every sum is exact, so the result is still bit-exact."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=3 * M + N + K)
+    assert_parity(run_gpu(A, B, variant=variant, stream_k=1), A, B, exact=True)
+
+
+@pytest.mark.parametrize("shape", [(777, 1000, 1536), (1024, 1024, 4096), (128, 2048, 16384)])
+def test_stream_k_tolerance(shape):
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "normal", seed=M + K)
+    for v in _variants():
+        assert_parity(run_gpu(A, B, variant=v, stream_k=1), A, B)
+
+
+def test_stream_k_plan_shape():
+    sms = num_sms()
+    p = G.gemm_f16_nt_plan_ex(4096, 4096, 4096, 2, 0, 1)
+    assert p.stream_k == 1 and p.workspace_bytes > 0
+    assert p.sk_iters == (p.num_tiles - p.dp_tiles) * p.k_blocks
+    assert p.dp_tiles % (p.grid // p.cluster) == 0
+
+
+def test_workspace_entry_point_rejects_small_workspace():
+    M = N = K = 4096
+    need = G.gemm_f16_nt_workspace_size(M, N, K)
+    if need == 0:
+        pytest.skip("automatic plan needs no workspace here")
+    a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    b = torch.zeros((N, K), dtype=torch.float16, device="cuda")
+    c = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    st = G.lib().gemm_f16_nt_ws(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), small.data_ptr(), need - 256,
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == G.GEMM_ERR_WORKSPACE
 
 
 # ------------------------------------------------------ structured operands
@@ -151,12 +197,19 @@ def test_side_stream_and_host_entry_point():
     G.gemm_f16_nt_host(a_h, b_h, c_h, a_d, b_d, c_d, stream=s)
     s.synchronize()
     assert_parity(c_h.view(torch.int16).numpy().view(np.uint16), A, B, exact=True)
+    ws = torch.empty(max(256, G.gemm_f16_nt_workspace_size(M, N, K)), dtype=torch.uint8, device="cuda")
+    c_h.zero_()
+    G.gemm_f16_nt_host(a_h, b_h, c_h, a_d, b_d, c_d, ws, stream=s)
+    s.synchronize()
+    assert_parity(c_h.view(torch.int16).numpy().view(np.uint16), A, B, exact=True)
 
 
 def test_plan_matches_device():
     p = G.gemm_f16_nt_plan(8192, 8192, 8192)
     assert p.num_sms == num_sms()
-    assert G.gemm_f16_nt_workspace_size(8192, 8192, 8192) == p.workspace_bytes == 0
+    assert G.gemm_f16_nt_workspace_size(8192, 8192, 8192) == p.workspace_bytes
+    if p.stream_k:
+        assert p.workspace_bytes >= p.grid * (p.block_m // p.cta_group) * p.block_n * 4
 
 
 # ------------------------------------------------------- full workloads
@@ -167,21 +220,24 @@ def _full(name):
     return w, A, B
 
 
+@pytest.mark.parametrize("use_ws", [False, True])
 @pytest.mark.parametrize("name", ["square_256", "ragged_3000x5000x4096"])
-def test_integer_workloads_bit_exact(name):
+def test_integer_workloads_bit_exact(name, use_ws):
     w, A, B = _full(name)
-    assert_parity(run_gpu(A, B), A, B, exact=True)
+    assert_parity(run_gpu(A, B, use_ws_entry=use_ws), A, B, exact=True)
 
 
+@pytest.mark.parametrize("use_ws", [False, True])
 @pytest.mark.parametrize("name", ["square_4096", "skinny_128x16384x16384"])
-def test_real_workloads_full_tolerance(name):
+def test_real_workloads_full_tolerance(name, use_ws):
     w, A, B = _full(name)
-    assert_parity(run_gpu(A, B), A, B)
+    assert_parity(run_gpu(A, B, use_ws_entry=use_ws), A, B)
 
 
-def test_square_8192_sampled():
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_square_8192_sampled(use_ws):
     w, A, B = _full("square_8192")
-    c = run_gpu(A, B)
+    c = run_gpu(A, B, use_ws_entry=use_ws)
     rng = np.random.Generator(np.random.PCG64(8192))
     rows = np.concatenate([rng.integers(0, 8192, size=6000), np.arange(8192), np.full(2048, 8191),
                            np.arange(128)])
