@@ -620,3 +620,58 @@ gemm_status_t gemm_f16_fast_divmod(uint32_t d, uint32_t n, uint32_t *q, uint32_t
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free form
+
+// Scratch of gemm_f16_nt_noalloc: the stream-K partial tiles and flags of
+// one call at a time, inside the library's device image.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_F16_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (host code must not pass the symbol itself to a kernel).
+gemm_status_t noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_f16_nt_noalloc(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
+                                             void *c, gemm_stream_t stream)
+{
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    st = check_pointers(m, n, k, a, b, c);
+    if (st != GEMM_OK) return st;
+    if (m == 0 || n == 0) return GEMM_OK;
+    gemm_f16_plan_t p;
+    st = device_plan(m, n, k, -1, 0, -1, &p);
+    if (st != GEMM_OK) return st;
+    if (p.workspace_bytes > uint64_t(GEMM_F16_STATIC_SCRATCH_BYTES)) return GEMM_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (p.workspace_bytes > 0) {
+        st = noalloc_scratch(&scratch);
+        if (st != GEMM_OK) return st;
+    }
+    return run_plan(p, a, b, c, scratch, size_t(GEMM_F16_STATIC_SCRATCH_BYTES), reinterpret_cast<cudaStream_t>(stream),
+                    ~0u, default_wait_limit(p.k_blocks));
+}

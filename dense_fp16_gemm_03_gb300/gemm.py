@@ -23,6 +23,9 @@ GEMM_ERR_CUDA = 8
 
 LIB_PATH = _build.LIB
 
+# size of the scratch array built into the library (GEMM_F16_STATIC_SCRATCH_BYTES)
+STATIC_SCRATCH_BYTES = 20 * 1024 * 1024
+
 
 class GemmError(RuntimeError):
     def __init__(self, status, where):
@@ -70,7 +73,7 @@ EXPORTED = [
     "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_plan_ex", "gemm_f16_nt_workspace_size",
     "gemm_f16_nt", "gemm_f16_nt_ws", "gemm_f16_nt_run", "gemm_f16_nt_host",
     "gemm_f16_take_device_error", "gemm_f16_raster_coord", "gemm_f16_fast_divmod",
-    "gemm_f16_nt_run_stall_test",
+    "gemm_f16_nt_run_stall_test", "gemm_f16_nt_noalloc",
 ]
 
 _lib = None
@@ -103,6 +106,7 @@ def lib():
         "gemm_f16_raster_coord": (ctypes.c_int, [i64, i64, i32, i64, pi64, pi64]),
         "gemm_f16_fast_divmod": (ctypes.c_int, [u32, u32, pu32, pu32]),
         "gemm_f16_nt_run_stall_test": (ctypes.c_int, [P, vp, vp, vp, u32, ctypes.c_longlong, vp]),
+        "gemm_f16_nt_noalloc": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -223,6 +227,20 @@ def gemm_f16_nt_run(plan, a, b, c, workspace=None, stream=None):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().gemm_f16_nt_run(ctypes.byref(plan), _ptr(a), _ptr(b), _ptr(c), _ptr(workspace), ws_bytes,
                                  _stream(stream)), "gemm_f16_nt_run")
+    return c
+
+
+def gemm_f16_nt_noalloc(a, b, c, stream=None):
+    """C = A . B^T with the library's built-in scratch array (allocates nothing).
+
+    For callers that may not allocate device memory; calls must not overlap
+    on the GPU (they share the one scratch array).  Make the first call on a
+    device before any stream capture.
+    """
+    m, n, k = _shape(a, b)
+    if tuple(c.shape) != (m, n) or not c.is_contiguous():
+        raise ValueError("c must be a contiguous float16 [M,N] tensor")
+    _check(lib().gemm_f16_nt_noalloc(m, n, k, _ptr(a), _ptr(b), _ptr(c), _stream(stream)), "gemm_f16_nt_noalloc")
     return c
 
 

@@ -201,6 +201,37 @@ gemm_status_t gemm_f16_raster_coord(int64_t tiles_m, int64_t tiles_n, int32_t ra
 gemm_status_t gemm_f16_fast_divmod(uint32_t d, uint32_t n, uint32_t *q, uint32_t *r);
 
 /*
+ * Allocation-free form (no counterpart on the reference pages).
+ *
+ * Some callers cannot allocate device memory at all: code embedded in a
+ * host process that owns every device allocation through its own pool (an
+ * inference server, a framework plugin), where a side allocation is
+ * forbidden or would break the host's memory accounting, and code on paths
+ * that must not call cudaMalloc/cudaFree because those calls can
+ * synchronize the device.  For them, gemm_f16_nt_noalloc computes the same
+ * product as gemm_f16_nt_ws with the automatic plan (stream-K tail when it
+ * pays) but takes its scratch -- the stream-K partial tiles and flags --
+ * from one array that lives inside this library's device image, of
+ * GEMM_F16_STATIC_SCRATCH_BYTES bytes; every GPU that loads the library
+ * holds that array until the process exits.  The caller still passes the
+ * operands and the output (device pointers, as for gemm_f16_nt).
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and keeps it; make that first call before any stream
+ * capture.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.  All calls share the one array and it keeps
+ * the last call's contents (the library clears the flags that must start at
+ * zero before every launch), so calls whose kernels overlap on the GPU --
+ * two streams, or two host threads -- race on it and give wrong results;
+ * serialize them.  A plan that needs more scratch than the array holds is
+ * rejected with GEMM_ERR_WORKSPACE before any launch (on a 152-SM GB300 the
+ * largest plan needs 19.0 MiB).  Other errors as for gemm_f16_nt.
+ */
+#define GEMM_F16_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
+gemm_status_t gemm_f16_nt_noalloc(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
+                                  void *c, gemm_stream_t stream);
+
+/*
  * Failure-detection hook for tests (no counterpart on the reference pages):
  * launches `plan` like gemm_f16_nt_run, except that the TMA producer of CTA 0
  * leaves its `skip_fill`-th ring-stage fill undone and every pipeline wait is

@@ -36,6 +36,12 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == set(G.EXPORTED)
 
 
+def test_static_scratch_size_matches_header(L):
+    text = open(os.path.join(ROOT, "include", "gemm_f16.h")).read()
+    m = re.search(r"#define GEMM_F16_STATIC_SCRATCH_BYTES \((\d+)u \* 1024u \* 1024u\)", text)
+    assert m and int(m.group(1)) * 1024 * 1024 == G.STATIC_SCRATCH_BYTES
+
+
 def test_status_strings(L):
     for s in range(9):
         assert G.status_string(s).startswith("GEMM_")
