@@ -71,6 +71,7 @@ const Variant kVariants[] = {
     GEMM_VARIANT(2, 256, 6, 1),  // 2: 256 x 256 tile on a CTA pair
     GEMM_VARIANT(2, 128, 8, 1),  // 3: 256 x 128 tile on a CTA pair
     GEMM_VARIANT(2, 256, 6, 2),  // 4: two pairs stacked along M share B by multicast (512 x 256 per cluster)
+    GEMM_VARIANT(2, 224, 6, 2),  // 5: as 4 with 224-column tiles (512 x 224 per cluster)
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -191,14 +192,30 @@ int32_t auto_raster_width(int64_t tiles_n)
     return int32_t(w < 1 ? 1 : w);
 }
 
-// Tile-shape choice, from measurement on GB300: the 256 x 256 CTA-pair
-// tile (variant 2) is fastest on every shape with more than 128 rows; a
-// single 128-row tile (M <= 128) leaves the second CTA of a pair idle, and
-// there the one-CTA 128 x 128 tile (variant 1) is fastest.
-int32_t auto_variant(int64_t m, int64_t n)
+// Fraction of the resident slots the data-parallel waves keep busy.
+double wave_efficiency(int64_t tiles, int64_t slots)
 {
-    (void)n;
-    return m <= 128 ? 1 : 2;
+    if (tiles <= 0 || slots <= 0) return 1.0;
+    const int64_t waves = (tiles + slots - 1) / slots;
+    return double(tiles) / double(waves * slots);
+}
+
+// Tile-shape choice, from interleaved measurements on GB300 under the power
+// cap (256 x 256 CTA-pair tiles balance the tensor core against shared-
+// memory bandwidth; narrower tiles measured slower on every workload):
+//  - M <= 128: one 128-row tile; a CTA pair's second CTA would idle, the
+//    single-CTA 128 x 128 tile (variant 1) is fastest;
+//  - M <= 256: the 256 x 256 pair tile (variant 2);
+//  - otherwise the pair tile when its waves keep >= 95% of the pair slots
+//    busy (8192^3), else two pairs sharing B by multicast (variant 4), which
+//    moves less data per flop but fits only whole clusters of four SMs.
+int32_t auto_variant(int64_t m, int64_t n, int32_t num_sms, const int32_t *slots_by_variant)
+{
+    if (m <= 128) return 1;
+    if (m <= 256) return 2;
+    const int64_t pair_slots = slots_by_variant ? slots_by_variant[2] : num_sms / 2;
+    const int64_t pair_tiles = ((m + 255) / 256) * ((n + 255) / 256);
+    return wave_efficiency(pair_tiles, pair_slots) >= 0.95 ? 2 : 4;
 }
 
 int64_t round_up(int64_t x, int64_t a)
@@ -217,27 +234,31 @@ int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
     return streamk_partials_bytes(grid, block_n) + round_up(grid * 4, 256);
 }
 
-// A stream-K tail pays when the data-parallel schedule would leave a last
-// wave of tiles noticeably short of the resident clusters.
+// A stream-K tail pays when the data-parallel schedule would leave the last
+// wave badly short of the resident clusters: measured, it wins when less
+// than about 86% of the slots are busy over the waves (ragged 3000x5000),
+// and loses above that, because under the power cap keeping the idle SMs of
+// a nearly full last wave busy costs clock for the whole launch.
 bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
 {
     if (k_blocks < 4 || num_tiles * k_blocks < 2 * slots) return false;
-    const int64_t waves = cdiv(num_tiles, slots);
-    return double(num_tiles) / double(waves * slots) < 0.98;
+    return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
 gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters_in,
-                        int32_t variant, int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out)
+                        int32_t variant, int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out,
+                        const int32_t *slots_by_variant = nullptr)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_shape(m, n, k);
     if (st != GEMM_OK) return st;
     if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
     if (variant >= kNumVariants || stream_k > 1) return GEMM_ERR_INVALID_ARG;
-    if (variant < 0) variant = auto_variant(m, n);
+    if (variant < 0) variant = auto_variant(m, n, num_sms, slots_by_variant);
     const Variant &var = kVariants[variant];
     const int32_t cs = var.cg * var.mc;  // CTAs per cluster
-    const int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / cs;
+    int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / cs;
+    if (slots_by_variant) max_clusters = slots_by_variant[variant];
     gemm_f16_plan_t p;
     memset(&p, 0, sizeof(p));
     p.variant = variant;
@@ -308,17 +329,18 @@ gemm_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
     return g_encode ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Row-major fp16 matrix of `rows` x `cols` (cols contiguous), 128-byte
-// swizzled boxes of box_cols x box_rows, zero fill outside the matrix.
+// Row-major fp16 matrix of `rows` x `cols` (cols contiguous), boxes of
+// box_cols x box_rows (128-byte swizzled unless `swizzle` is false), zero
+// fill outside the matrix.
 gemm_status_t encode_matrix(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *ptr,
-                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows)
+                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows, bool swizzle = true)
 {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
 }
@@ -378,6 +400,10 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     if (st != GEMM_OK) return st;
     st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
     if (st != GEMM_OK) return st;
+    if (var.bn % 64 != 0) {
+        st = encode_matrix(enc, &params.tmap_c32, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, false);
+        if (st != GEMM_OK) return st;
+    }
     params.raster = make_raster(uint32_t(plan.tiles_m), uint32_t(plan.tiles_n), uint32_t(plan.raster_width));
     params.m = uint32_t(plan.m);
     params.n = uint32_t(plan.n);
@@ -474,8 +500,7 @@ gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int3
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
-    const int32_t v = variant < 0 ? auto_variant(m, n) : variant;
-    return make_plan(m, n, k, dev->num_sms, dev->max_clusters[v], v, raster_width, stream_k, out);
+    return make_plan(m, n, k, dev->num_sms, 0, variant, raster_width, stream_k, out, dev->max_clusters);
 }
 
 }  // namespace

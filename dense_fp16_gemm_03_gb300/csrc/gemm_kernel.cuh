@@ -58,6 +58,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -84,7 +86,8 @@ enum : uint32_t {
 struct KernelParams {
     CUtensorMap tmap_a;   // A [M, K]: box {64, 128}
     CUtensorMap tmap_b;   // B [N, K]: box {64, BN / CG}
-    CUtensorMap tmap_c;   // C [M, N]: box {64, 32}
+    CUtensorMap tmap_c;   // C [M, N]: box {64, 32}, 128-byte swizzle
+    CUtensorMap tmap_c32; // C [M, N]: box {32, 32}, no swizzle (last chunk of a tile N % 64 == 32)
     Raster raster;
     uint32_t m, n, k;
     uint32_t num_tiles;
@@ -103,7 +106,9 @@ template <int CG, int BN, int STAGES, int MC = 1>
 struct KernelCfg {
     static_assert(CG == 1 || CG == 2, "cta group");
     static_assert(MC == 1 || (CG == 2 && (MC == 2 || MC == 4)), "B multicast needs CTA pairs");
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N");
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile N");
+    static constexpr int kFullChunks = BN / 64;      // 64-column epilogue chunks
+    static constexpr bool kTail = (BN % 64) != 0;   // plus one 32-column chunk
     static constexpr int kCS = CG * MC;             // CTAs per cluster
     static constexpr int kBM = 128 * CG;            // MMA M (one pair)
     static constexpr int kBMCluster = kBM * MC;     // output rows per scheduling unit
@@ -121,8 +126,10 @@ struct KernelCfg {
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
-    static constexpr int kTmemCols = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
+    static constexpr int kAccCols = (BN + 63) / 64 * 64;  // accumulator buffer stride (64-column aligned)
+    static constexpr int kTmemCols = (2 * kAccCols <= 128) ? 128 : (2 * kAccCols <= 256 ? 256 : 512);
     static_assert(kBBytes % 1024 == 0 && kABytes % 1024 == 0 && (kBSlice * 128) % 1024 == 0, "swizzle atoms");
+    static_assert(BN % (16 * CG) == 0, "MMA N");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
 
@@ -251,6 +258,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         ptx::prefetch_tmap(&p.tmap_a);
         ptx::prefetch_tmap(&p.tmap_b);
         ptx::prefetch_tmap(&p.tmap_c);
+        if constexpr (Cfg::kTail) ptx::prefetch_tmap(&p.tmap_c32);
     }
     if (warp == 1) {
         ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
@@ -316,7 +324,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 if (!wait_bounded<CG>(bar_acc_empty(acc), acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty))
                     return false;
                 ptx::tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols;
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb) {
                     if (!wait_bounded<CG>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
                     ptx::tc_fence_after_sync();
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             const bool all_ok = split ? ptx::named_barrier_and(1, 32 * kEpiWarps, ok) : __all_sync(0xffffffffu, ok);
             if (!all_ok) return false;
             ptx::tc_fence_after_sync();
-            const uint32_t acc_col = tmem_base + acc * BN + lane_sel;
+            const uint32_t acc_col = tmem_base + acc * Cfg::kAccCols + lane_sel;
             // Partial-tile layout in the workspace: per warp quarter and 64-column chunk, 16 float4
             // slots x 32 lanes, so every warp-wide 16-byte access is one contiguous 512-byte run.
             const uint32_t piece = quarter * 32u * BN + lane * 4u;
@@ -384,18 +392,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 // ---- publish this partial tile; the owner of the tile adds it
                 float *slot = p.partials + size_t(blockIdx.x) * kSlotFloats + piece;
                 if (row0 < p.m) {
-#pragma unroll 1
-                    for (int c = 0; c < BN / kStoreCols; ++c) {
-                        if (col0 + uint32_t(c * kStoreCols) >= p.n) break;
-                        uint32_t r[64];
-                        ptx::tmem_ld_32x32b_x64_wait(acc_col + uint32_t(c * kStoreCols), r);
+                    auto publish = [&](auto width, int c) {
+                        constexpr int W = decltype(width)::value;
+                        if (col0 + uint32_t(c * kStoreCols) >= p.n) return;
+                        uint32_t r[W];
+                        if constexpr (W == 64) ptx::tmem_ld_32x32b_x64_wait(acc_col + uint32_t(c * kStoreCols), r);
+                        else ptx::tmem_ld_32x32b_x32_wait(acc_col + uint32_t(c * kStoreCols), r);
                         float *dst = slot + c * kChunkFloats;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
+                        for (int j = 0; j < W / 4; ++j)
                             ptx::st_global_cg_f4(dst + j * 128, __uint_as_float(r[4 * j]),
                                                  __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
                                                  __uint_as_float(r[4 * j + 3]));
-                    }
+                    };
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::kFullChunks; ++c) publish(std::integral_constant<int, 64>{}, c);
+                    if constexpr (Cfg::kTail) publish(std::integral_constant<int, 32>{}, Cfg::kFullChunks);
                 }
                 __threadfence();
                 ptx::named_barrier_sync(1, 32 * kEpiWarps);
@@ -425,18 +437,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     ptx::named_barrier_sync(1, 32 * kEpiWarps);
                 }
                 if (row0 < p.m) {
-#pragma unroll 1
-                    for (int c = 0; c < BN / kStoreCols; ++c) {
+                    auto store = [&](auto width, int c) {
+                        constexpr int W = decltype(width)::value;
                         const uint32_t col = col0 + uint32_t(c * kStoreCols);
-                        if (col >= p.n) break;
-                        uint32_t r[64];
-                        ptx::tmem_ld_32x32b_x64_wait(acc_col + uint32_t(c * kStoreCols), r);
+                        if (col >= p.n) return;
+                        uint32_t r[W];
+                        if constexpr (W == 64) ptx::tmem_ld_32x32b_x64_wait(acc_col + uint32_t(c * kStoreCols), r);
+                        else ptx::tmem_ld_32x32b_x32_wait(acc_col + uint32_t(c * kStoreCols), r);
                         for (uint32_t w = first_w; w < last_w; ++w) {
                             if (sk_begin(p, w, num_clusters) >= sk_begin(p, w + 1, num_clusters)) continue;
                             const float *src =
                                 p.partials + size_t(w * CS + cta_rank) * kSlotFloats + piece + c * kChunkFloats;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
+                            for (int j = 0; j < W / 4; ++j) {
                                 const float4 v = ptx::ld_global_cg_f4(src + j * 128);
                                 r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
                                 r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
@@ -447,24 +460,39 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                         const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
                         if (lane == 0) ptx::bulk_wait_group_read<1>();  // this buffer's previous store has read it
                         __syncwarp();
-                        const uint32_t row_addr = buf + lane * 128u;
+                        if constexpr (W == 64) {
+                            const uint32_t row_addr = buf + lane * 128u;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t w0 = pack_half2(r[8 * j + 0], r[8 * j + 1]);
-                            const uint32_t w1 = pack_half2(r[8 * j + 2], r[8 * j + 3]);
-                            const uint32_t w2 = pack_half2(r[8 * j + 4], r[8 * j + 5]);
-                            const uint32_t w3 = pack_half2(r[8 * j + 6], r[8 * j + 7]);
-                            // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r mod 8)
-                            ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), w0, w1, w2, w3);
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t w0 = pack_half2(r[8 * j + 0], r[8 * j + 1]);
+                                const uint32_t w1 = pack_half2(r[8 * j + 2], r[8 * j + 3]);
+                                const uint32_t w2 = pack_half2(r[8 * j + 4], r[8 * j + 5]);
+                                const uint32_t w3 = pack_half2(r[8 * j + 6], r[8 * j + 7]);
+                                // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r mod 8)
+                                ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), w0, w1, w2, w3);
+                            }
+                        } else {
+                            const uint32_t row_addr = buf + lane * 64u;  // unswizzled 64-byte rows
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                ptx::st_shared_v4(row_addr + (uint32_t(j) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                                                  pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                                                  pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                                                  pack_half2(r[8 * j + 6], r[8 * j + 7]));
                         }
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmap_c, buf, int32_t(col), int32_t(row0));
+                            ptx::tma_store_2d(W == 64 ? static_cast<const void *>(&p.tmap_c)
+                                                      : static_cast<const void *>(&p.tmap_c32),
+                                              buf, int32_t(col), int32_t(row0));
                             ptx::bulk_commit_group();
                         }
                         ++stores;
-                    }
+                    };
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::kFullChunks; ++c) store(std::integral_constant<int, 64>{}, c);
+                    if constexpr (Cfg::kTail) store(std::integral_constant<int, 32>{}, Cfg::kFullChunks);
                 }
             }
             ptx::tc_fence_before_sync();

@@ -30,7 +30,7 @@ def _variants():
 
 # ------------------------------------------------------------------ small
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
 def test_square_256_exact_every_variant(variant):
     w = inputs.BY_NAME["square_256"]
     A, B = inputs.workload_operands(w)
@@ -48,7 +48,7 @@ RAGGED = [(1, 8, 8), (3, 8, 16), (129, 264, 72), (128, 256, 64), (257, 136, 200)
 
 
 @pytest.mark.parametrize("shape", RAGGED)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
 def test_ragged_exact(shape, variant):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "eighths", seed=M + 7 * N + 13 * K)
@@ -79,7 +79,7 @@ SK_SHAPES = [(640, 1032, 520), (1000, 1000, 1000), (300, 520, 4096), (128, 256, 
 
 
 @pytest.mark.parametrize("shape", SK_SHAPES)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
 def test_stream_k_exact(shape, variant):
     """Split tiles are summed from fp32 partials; on integer-valued operands
     every partial and every sum is exact, so the result is still bit-exact."""
@@ -105,10 +105,9 @@ def test_stream_k_plan_shape():
 
 
 def test_workspace_entry_point_rejects_small_workspace():
-    M = N = K = 4096
+    M, N, K = 3000, 5000, 4096
     need = G.gemm_f16_nt_workspace_size(M, N, K)
-    if need == 0:
-        pytest.skip("automatic plan needs no workspace here")
+    assert need > 0                               # the automatic plan has a stream-K tail here
     a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     b = torch.zeros((N, K), dtype=torch.float16, device="cuda")
     c = torch.zeros((M, N), dtype=torch.float16, device="cuda")
