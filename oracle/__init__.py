@@ -35,6 +35,12 @@ def lib():
         L.oracle_gemm_nt.argtypes = [i64, i64, i64, u16p, u16p, u16p, f64p, f64p]
         L.oracle_gemm_nt_entries.restype = ctypes.c_int
         L.oracle_gemm_nt_entries.argtypes = [i64, i64, i64, u16p, u16p, i64, i64p, i64p, u16p, f64p, f64p]
+        L.oracle_gemm_nn_f32.restype = ctypes.c_int
+        L.oracle_gemm_nn_f32.argtypes = [i64, i64, i64, u16p, u16p, ctypes.c_void_p, f64p, f64p]
+        L.oracle_gemm_nn_f32_entries.restype = ctypes.c_int
+        L.oracle_gemm_nn_f32_entries.argtypes = [i64, i64, i64, u16p, u16p, i64, i64p, i64p, ctypes.c_void_p,
+                                                 f64p, f64p]
+        L.oracle_f64_to_f32_array.argtypes = [i64, f64p, ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -108,8 +114,51 @@ def gemm_nt_entries(A, B, rows, cols, want_exact=False):
     return (c, absum, exact) if want_exact else (c, absum)
 
 
+def gemm_nn_f32(A, B_kn, want_exact=False):
+    """D = A . B with A [M,K] and B [K,N] fp16 (or uint16 bits), fp32 result.
+
+    Returns (D float32 [M,N], absum float64 [M,N]) and, if want_exact, the
+    unrounded double sums.
+    """
+    a, b = _bits(A), _bits(B_kn)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError("A must be [M,K] and B [K,N]")
+    M, K = a.shape
+    N = b.shape[1]
+    d = np.empty((M, N), dtype=np.float32)
+    absum = np.empty((M, N), dtype=np.float64)
+    exact = np.empty((M, N), dtype=np.float64) if want_exact else None
+    rc = lib().oracle_gemm_nn_f32(M, N, K, _ptr(a), _ptr(b), _ptr(d), _ptr(absum),
+                                  _ptr(exact) if want_exact else None)
+    if rc != 0:
+        raise MemoryError("oracle_gemm_nn_f32 failed (%d)" % rc)
+    return (d, absum, exact) if want_exact else (d, absum)
+
+
+def gemm_nn_f32_entries(A, B_kn, rows, cols):
+    a, b = _bits(A), _bits(B_kn)
+    M, K = a.shape
+    N = b.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    d = np.empty(rows.shape, dtype=np.float32)
+    absum = np.empty(rows.shape, dtype=np.float64)
+    rc = lib().oracle_gemm_nn_f32_entries(M, N, K, _ptr(a), _ptr(b), rows.size, _ptr(rows), _ptr(cols), _ptr(d),
+                                          _ptr(absum), None)
+    if rc != 0:
+        raise ValueError("oracle_gemm_nn_f32_entries failed (%d)" % rc)
+    return d, absum
+
+
+def f64_to_f32(values):
+    values = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(values.shape, dtype=np.float32)
+    lib().oracle_f64_to_f32_array(values.size, _ptr(values), _ptr(out))
+    return out
+
+
 def num_threads():
     return int(lib().oracle_num_threads())
 
 
-from .tolerance import check_parity, ulp16  # noqa: E402,F401
+from .tolerance import check_parity, check_parity_f32, ulp16, ulp32  # noqa: E402,F401

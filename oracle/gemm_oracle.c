@@ -27,6 +27,9 @@
  * binary16 interchange format (1 sign bit, 5 exponent bits with bias 15,
  * 10 fraction bits) and its round-to-nearest-ties-to-even rule.
  *
+ * A second entry computes the layout of "wgmma_gemm.cu" (B as [K, N],
+ * fp32 result); see oracle_gemm_nn_f32.
+ *
  * Parity pins (checked by tests marked "not gpu"): exhaustive conversion
  * checks against an independent library, brute force with exact rational
  * arithmetic, identity and permutation operands, rank-1 closed forms,
@@ -180,6 +183,68 @@ int oracle_gemm_nt_entries(int64_t M, int64_t N, int64_t K, const uint16_t *A,
     }
     free(decode);
     return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* The layout of the "wgmma_gemm.cu" page (function gemmCpu and the D   */
+/* store of its kernel): D[M,N] = A[M,K] . B[K,N] with B row-major      */
+/* [K,N] (N contiguous) and an fp32 result:                             */
+/*     D[i][j] = fp32_rne( sum_{k} double(A[i][k]) * double(B[k][j]) )  */
+/* summed in double in natural k order; the cast to float is the C      */
+/* language's IEEE 754 double -> binary32 conversion (round to nearest  */
+/* even in the default floating-point environment).  absum as above.    */
+static void dot_entry_kn(int64_t N, int64_t K, const uint16_t *a_row, const uint16_t *b_col,
+                         const double *decode, float *d_out, double *absum_out, double *sum_out)
+{
+    double sum = 0.0;
+    double abs_sum = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double product = decode[a_row[k]] * decode[b_col[k * N]];
+        sum += product;
+        abs_sum += fabs(product);
+    }
+    *d_out = (float)sum;
+    if (absum_out) *absum_out = abs_sum;
+    if (sum_out) *sum_out = sum;
+}
+
+int oracle_gemm_nn_f32(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
+                       float *D, double *absum, double *exact)
+{
+    double *decode = make_decode_table();
+    if (!decode) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            dot_entry_kn(N, K, A + i * K, B + j, decode, D + i * N + j,
+                         absum ? absum + i * N + j : NULL, exact ? exact + i * N + j : NULL);
+        }
+    }
+    free(decode);
+    return 0;
+}
+
+int oracle_gemm_nn_f32_entries(int64_t M, int64_t N, int64_t K, const uint16_t *A, const uint16_t *B,
+                               int64_t count, const int64_t *rows, const int64_t *cols, float *D,
+                               double *absum, double *exact)
+{
+    for (int64_t e = 0; e < count; ++e) {
+        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -2;
+    }
+    double *decode = make_decode_table();
+    if (!decode) return -1;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t e = 0; e < count; ++e) {
+        dot_entry_kn(N, K, A + rows[e] * K, B + cols[e], decode, D + e, absum ? absum + e : NULL,
+                     exact ? exact + e : NULL);
+    }
+    free(decode);
+    return 0;
+}
+
+void oracle_f64_to_f32_array(int64_t count, const double *src, float *dst)
+{
+    for (int64_t i = 0; i < count; ++i) dst[i] = (float)src[i];
 }
 
 int oracle_num_threads(void)

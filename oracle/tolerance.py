@@ -74,3 +74,36 @@ def check_parity(c_gpu_bits, c_ref_bits, absum, rel=1e-3, index_shape=None):
     fin = np.isfinite(g) & finite_ref
     max_abs = float(err[fin].max()) if fin.any() else 0.0
     return ParityReport(bad.size == 0, int(bad.size), first, worst, max_abs, g.size)
+
+
+def ulp32(ref_values):
+    """binary32 spacing at |x| for finite double values x: 2^(e-23) for a
+    normal |x| in [2^e, 2^(e+1)), 2^-149 below 2^-126."""
+    x = np.abs(np.asarray(ref_values, dtype=np.float64))
+    _, e2 = np.frexp(x)
+    e = e2.astype(np.int64) - 1
+    spacing = np.ldexp(1.0, (np.maximum(e, -126) - 23).astype(np.int64))
+    return np.where(x < 2.0 ** -126, 2.0 ** -149, spacing)
+
+
+def check_parity_f32(d_gpu, d_ref, absum, rel=1e-3, index_shape=None):
+    """The fp32-output form of the bound: |d_gpu - d_ref| <= 1e-3 * sum|a*b|
+    + ulp32(d_ref) for every element; Inf/NaN from the GPU fails."""
+    g = np.asarray(d_gpu, dtype=np.float32).astype(np.float64).ravel()
+    r = np.asarray(d_ref, dtype=np.float32).astype(np.float64).ravel()
+    s = np.asarray(absum, dtype=np.float64).ravel()
+    bound = rel * s + ulp32(r)
+    err = np.abs(g - r)
+    ok_elem = np.isfinite(g) & (err <= bound)
+    bad = np.flatnonzero(~ok_elem)
+    first = None
+    if bad.size:
+        idx = int(bad[0])
+        pos = np.unravel_index(idx, index_shape) if index_shape is not None else idx
+        first = (pos, float(g[idx]), float(r[idx]), float(bound[idx]))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    ratio = np.where(np.isfinite(g), ratio, np.inf)
+    fin = np.isfinite(g)
+    return ParityReport(bad.size == 0, int(bad.size), first, float(ratio.max()) if ratio.size else 0.0,
+                        float(err[fin].max()) if fin.any() else 0.0, g.size)

@@ -256,3 +256,86 @@ def test_check_parity_bounds():
     for bad in (np.inf, np.nan):
         g = np.array([bad, 2.0, -0.5, 0.0]).astype(np.float16).view(np.uint16)
         assert not oracle.check_parity(g, ref, np.full(4, 1e9)).ok
+
+
+# --------------------------------------------------------------------------
+# the fp32-output product with B stored [K, N] ("wgmma_gemm.cu" layout)
+
+def test_f64_to_f32_golden_cases():
+    path = os.path.join(GOLDEN, "f32_rounding_cases.txt")
+    n = 0
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        src, expect = line.split()[:2]
+        got = float(oracle.f64_to_f32(np.array([float.fromhex(src)]))[0])
+        assert got == float.fromhex(expect), (src, got.hex(), expect)
+        n += 1
+    assert n >= 10
+
+
+@pytest.mark.parametrize("shape", [(37, 53, 200), (64, 64, 256), (9, 130, 1000)])
+def test_nn_f32_integer_operands_exact(shape):
+    M, N, K = shape
+    A, Bnk = inputs.make_operands(M, N, K, "eighths", seed=M + 3 * N)
+    B = np.ascontiguousarray(Bnk.T)                 # [K, N]
+    Ai = (A.astype(np.float64) * 8).astype(np.int64)
+    Bi = (B.astype(np.float64) * 8).astype(np.int64)
+    D, absum = oracle.gemm_nn_f32(A, B)
+    assert D.dtype == np.float32
+    assert np.array_equal(D, ((Ai @ Bi).astype(np.float64) / 64.0).astype(np.float32))
+    assert np.array_equal(absum, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64) / 64.0)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_nn_f32_brute_force_exact_rationals(seed):
+    rng = np.random.Generator(np.random.PCG64(500 + seed))
+    M, N, K = (int(v) for v in rng.integers(1, 14, size=3))
+    A = _random_moderate_f16(rng, (M, K))
+    B = _random_moderate_f16(rng, (K, N))
+    D, absum, exact = oracle.gemm_nn_f32(A, B, want_exact=True)
+    for i in range(M):
+        for j in range(N):
+            s = sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(K))
+            assert Fraction(exact[i, j]) == s
+            assert D[i, j] == np.float32(float(s))
+
+
+def test_nn_f32_agrees_with_nt_sums():
+    """D = A . B and C = A . (B^T)^T are the same sums: the unrounded double
+    results of the two oracle entries coincide, and the fp16 result is the
+    fp16 rounding of the same value."""
+    rng = np.random.Generator(np.random.PCG64(9))
+    A = (rng.standard_normal((31, 96)) / 4).astype(np.float16)
+    Bkn = (rng.standard_normal((96, 45)) / 4).astype(np.float16)
+    D, absum_nn, exact_nn = oracle.gemm_nn_f32(A, Bkn, want_exact=True)
+    C, absum_nt, exact_nt = oracle.gemm_nt(A, np.ascontiguousarray(Bkn.T), want_exact=True)
+    assert np.array_equal(exact_nn, exact_nt) and np.array_equal(absum_nn, absum_nt)
+    assert np.array_equal(oracle.f64_to_f16(exact_nn), C)
+    assert np.array_equal(D, exact_nn.astype(np.float32))
+
+
+def test_nn_f32_identity_and_entries():
+    rng = np.random.Generator(np.random.PCG64(10))
+    A = rng.standard_normal((20, 48)).astype(np.float16)
+    D, _ = oracle.gemm_nn_f32(A, inputs.identity(48))          # B = I: D = A exactly
+    assert np.array_equal(D, A.astype(np.float32))
+    B = rng.standard_normal((48, 33)).astype(np.float16)
+    D, _ = oracle.gemm_nn_f32(inputs.identity(48), B)          # A = I: D = B exactly
+    assert np.array_equal(D, B.astype(np.float32))
+    D, absum = oracle.gemm_nn_f32(A, B)
+    rows, cols = rng.integers(0, 20, size=50), rng.integers(0, 33, size=50)
+    De, ae = oracle.gemm_nn_f32_entries(A, B, rows, cols)
+    assert np.array_equal(De, D[rows, cols]) and np.array_equal(ae, absum[rows, cols])
+
+
+def test_check_parity_f32_bounds():
+    ref = np.array([1.0, -2.0, 0.0], dtype=np.float32)
+    ok = np.array([1.0 + 2 ** -23, -2.0 + 2 ** -22, 2 ** -149], dtype=np.float32)
+    assert oracle.check_parity_f32(ok, ref, np.zeros(3)).ok
+    bad = np.array([1.0 + 2 ** -21, -2.0, 0.0], dtype=np.float32)
+    rep = oracle.check_parity_f32(bad, ref, np.zeros(3))
+    assert not rep.ok and rep.first[0] == 0
+    assert oracle.check_parity_f32(bad, ref, np.array([0.01, 0, 0])).ok
+    assert oracle.ulp32(np.array([1.0]))[0] == 2.0 ** -23
