@@ -30,19 +30,21 @@ constexpr int kMaxDevices = 64;
 // ------------------------------------------------------------ variants
 
 struct Variant {
-    int cg, bn, stages, mc, smem;
+    int cg, bn, stages, mc;
+    int layout;  // 0: B [N,K], fp16 C; 1: B [K,N], fp32 D
+    int smem;
     const void *fn;
     cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
 };
 
-template <int CG, int BN, int ST, int MC>
+template <int CG, int BN, int ST, int MC, bool BK, bool CF>
 cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(unsigned(plan.grid), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC>::kSmemBytes);
+    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC, BK, CF>::kSmemBytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     int na = 0;
@@ -55,15 +57,17 @@ cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &para
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC>, params);
+    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF>, params);
 }
 
-#define GEMM_VARIANT(CG, BN, ST, MC)                                                                     \
-    Variant                                                                                              \
-    {                                                                                                    \
-        CG, BN, ST, MC, KernelCfg<CG, BN, ST, MC>::kSmemBytes,                                           \
-            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC>), &launch_variant<CG, BN, ST, MC> \
+#define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF)                                                              \
+    Variant                                                                                                 \
+    {                                                                                                       \
+        CG, BN, ST, MC, (BK ? 0 : 1), KernelCfg<CG, BN, ST, MC, BK, CF>::kSmemBytes,                        \
+            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF>),                    \
+            &launch_variant<CG, BN, ST, MC, BK, CF>                                                         \
     }
+#define GEMM_VARIANT(CG, BN, ST, MC) GEMM_VARIANT_L(CG, BN, ST, MC, true, true)
 
 const Variant kVariants[] = {
     GEMM_VARIANT(1, 256, 4, 1),  // 0: 128 x 256 tile, one CTA
@@ -72,6 +76,9 @@ const Variant kVariants[] = {
     GEMM_VARIANT(2, 128, 8, 1),  // 3: 256 x 128 tile on a CTA pair
     GEMM_VARIANT(2, 256, 6, 2),  // 4: two pairs stacked along M share B by multicast (512 x 256 per cluster)
     GEMM_VARIANT(2, 224, 6, 2),  // 5: as 4 with 224-column tiles (512 x 224 per cluster)
+    // B stored [K, N] (MN-major operand), fp32 result
+    GEMM_VARIANT_L(1, 128, 6, 1, false, false),  // 6: 128 x 128 tile, one CTA
+    GEMM_VARIANT_L(2, 256, 6, 1, false, false),  // 7: 256 x 256 tile on a CTA pair
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -209,8 +216,9 @@ double wave_efficiency(int64_t tiles, int64_t slots)
 //  - otherwise the pair tile when its waves keep >= 95% of the pair slots
 //    busy (8192^3), else two pairs sharing B by multicast (variant 4), which
 //    moves less data per flop but fits only whole clusters of four SMs.
-int32_t auto_variant(int64_t m, int64_t n, int32_t num_sms, const int32_t *slots_by_variant)
+int32_t auto_variant(int64_t m, int64_t n, int32_t num_sms, const int32_t *slots_by_variant, int32_t layout)
 {
+    if (layout == 1) return m <= 128 ? 6 : 7;  // B stored [K, N], fp32 result
     if (m <= 128) return 1;
     if (m <= 256) return 2;
     const int64_t pair_slots = slots_by_variant ? slots_by_variant[2] : num_sms / 2;
@@ -247,15 +255,16 @@ bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
 
 gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters_in,
                         int32_t variant, int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out,
-                        const int32_t *slots_by_variant = nullptr)
+                        const int32_t *slots_by_variant = nullptr, int32_t layout = -1)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_shape(m, n, k);
     if (st != GEMM_OK) return st;
     if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
-    if (variant >= kNumVariants || stream_k > 1) return GEMM_ERR_INVALID_ARG;
-    if (variant < 0) variant = auto_variant(m, n, num_sms, slots_by_variant);
+    if (variant >= kNumVariants || stream_k > 1 || layout > 1) return GEMM_ERR_INVALID_ARG;
+    if (variant < 0) variant = auto_variant(m, n, num_sms, slots_by_variant, layout < 0 ? 0 : layout);
     const Variant &var = kVariants[variant];
+    if (layout >= 0 && var.layout != layout) return GEMM_ERR_INVALID_ARG;
     const int32_t cs = var.cg * var.mc;  // CTAs per cluster
     int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / cs;
     if (slots_by_variant) max_clusters = slots_by_variant[variant];
@@ -267,6 +276,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.block_n = var.bn;
     p.block_k = kBlockK;
     p.stages = var.stages;
+    p.layout = var.layout;
     p.m = m;
     p.n = n;
     p.k = k;
@@ -329,17 +339,19 @@ gemm_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
     return g_encode ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Row-major fp16 matrix of `rows` x `cols` (cols contiguous), boxes of
-// box_cols x box_rows (128-byte swizzled unless `swizzle` is false), zero
-// fill outside the matrix.
+// Row-major fp16 (or, with elem_bytes 4, fp32) matrix of `rows` x `cols`
+// (cols contiguous), boxes of box_cols x box_rows (128-byte swizzled unless
+// `swizzle` is false), zero fill outside the matrix.
 gemm_status_t encode_matrix(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *ptr,
-                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows, bool swizzle = true)
+                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows, bool swizzle = true,
+                            uint32_t elem_bytes = 2)
 {
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {cols * elem_bytes};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+    const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
@@ -357,8 +369,10 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
+    if (plan.variant < 0 || plan.variant >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+    const size_t c_elem = kVariants[plan.variant].layout == 1 ? 4u : 2u;
     if (plan.k == 0) {
-        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * 2u, stream) != cudaSuccess) {
+        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * c_elem, stream) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
@@ -395,12 +409,19 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     memset(&params, 0, sizeof(params));
     st = encode_matrix(enc, &params.tmap_a, a, uint64_t(plan.m), uint64_t(plan.k), kBlockK, 128);
     if (st != GEMM_OK) return st;
-    st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.n), uint64_t(plan.k), kBlockK,
-                       uint32_t(var.bn / var.cg / var.mc));
+    if (var.layout == 0) {
+        st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.n), uint64_t(plan.k), kBlockK,
+                           uint32_t(var.bn / var.cg / var.mc));
+        if (st != GEMM_OK) return st;
+        st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
+    } else {
+        // B [K, N]: 64-column boxes of 64 K rows; D [M, N] fp32: 32-column boxes
+        st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.k), uint64_t(plan.n), 64, kBlockK);
+        if (st != GEMM_OK) return st;
+        st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, true, 4);
+    }
     if (st != GEMM_OK) return st;
-    st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
-    if (st != GEMM_OK) return st;
-    if (var.bn % 64 != 0) {
+    if (var.bn % 64 != 0 && var.layout == 0) {
         st = encode_matrix(enc, &params.tmap_c32, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, false);
         if (st != GEMM_OK) return st;
     }
@@ -469,9 +490,11 @@ int32_t gemm_f16_variant_count(void)
 }
 
 gemm_status_t gemm_f16_variant_info(int32_t v, int32_t *cta_group, int32_t *block_n, int32_t *stages,
-                                    int32_t *smem_bytes)
+                                    int32_t *smem_bytes, int32_t *cluster, int32_t *layout)
 {
     if (v < 0 || v >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+    if (cluster) *cluster = kVariants[v].cg * kVariants[v].mc;
+    if (layout) *layout = kVariants[v].layout;
     if (cta_group) *cta_group = kVariants[v].cg;
     if (block_n) *block_n = kVariants[v].bn;
     if (stages) *stages = kVariants[v].stages;
@@ -491,7 +514,7 @@ namespace {
 
 // Plan for the current device; arguments as in gemm_f16_nt_plan_for.
 gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int32_t raster_width, int32_t stream_k,
-                          gemm_f16_plan_t *out)
+                          gemm_f16_plan_t *out, int32_t layout = 0)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_shape(m, n, k);
@@ -500,7 +523,7 @@ gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int3
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
-    return make_plan(m, n, k, dev->num_sms, 0, variant, raster_width, stream_k, out, dev->max_clusters);
+    return make_plan(m, n, k, dev->num_sms, 0, variant, raster_width, stream_k, out, dev->max_clusters, layout);
 }
 
 }  // namespace
@@ -564,6 +587,33 @@ gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const 
     if (!plan) return GEMM_ERR_INVALID_ARG;
     return run_plan(*plan, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
                     default_wait_limit(plan->k_blocks));
+}
+
+gemm_status_t gemm_f16_nn_f32_plan_ex(int64_t m, int64_t n, int64_t k, int32_t variant, int32_t raster_width,
+                                      int32_t stream_k, gemm_f16_plan_t *out)
+{
+    return device_plan(m, n, k, variant, raster_width, stream_k, out, 1);
+}
+
+gemm_status_t gemm_f16_nn_f32_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *d,
+                                 void *workspace, size_t ws_bytes, gemm_stream_t stream)
+{
+    gemm_status_t st = check_shape(m, n, k);
+    if (st != GEMM_OK) return st;
+    st = check_pointers(m, n, k, a, b, d);
+    if (st != GEMM_OK) return st;
+    if (m == 0 || n == 0) return GEMM_OK;
+    gemm_f16_plan_t p;
+    st = device_plan(m, n, k, -1, 0, workspace ? -1 : 0, &p, 1);
+    if (st != GEMM_OK) return st;
+    return run_plan(p, a, b, d, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                    default_wait_limit(p.k_blocks));
+}
+
+gemm_status_t gemm_f16_nn_f32(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *d,
+                              gemm_stream_t stream)
+{
+    return gemm_f16_nn_f32_ws(m, n, k, a, b, d, nullptr, 0, stream);
 }
 
 // Failure-detection hook: the producer of CTA 0 leaves fill number

@@ -86,7 +86,7 @@ enum : uint32_t {
 struct KernelParams {
     CUtensorMap tmap_a;   // A [M, K]: box {64, 128}
     CUtensorMap tmap_b;   // B [N, K]: box {64, BN / CG}
-    CUtensorMap tmap_c;   // C [M, N]: box {64, 32}, 128-byte swizzle
+    CUtensorMap tmap_c;   // C [M, N]: fp16 box {64, 32} (fp32 box {32, 32}), 128-byte swizzle
     CUtensorMap tmap_c32; // C [M, N]: box {32, 32}, no swizzle (last chunk of a tile N % 64 == 32)
     Raster raster;
     uint32_t m, n, k;
@@ -102,7 +102,7 @@ struct KernelParams {
     uint32_t *error_word;
 };
 
-template <int CG, int BN, int STAGES, int MC = 1>
+template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true>
 struct KernelCfg {
     static_assert(CG == 1 || CG == 2, "cta group");
     static_assert(MC == 1 || (CG == 2 && (MC == 2 || MC == 4)), "B multicast needs CTA pairs");
@@ -130,6 +130,9 @@ struct KernelCfg {
     static constexpr int kTmemCols = (2 * kAccCols <= 128) ? 128 : (2 * kAccCols <= 256 ? 256 : 512);
     static_assert(kBBytes % 1024 == 0 && kABytes % 1024 == 0 && (kBSlice * 128) % 1024 == 0, "swizzle atoms");
     static_assert(BN % (16 * CG) == 0, "MMA N");
+    // B stored [K, N] (MN-major operand): whole 64-column swizzle atoms, no multicast slices
+    static_assert(B_KMAJOR || (MC == 1 && kBNCta % 64 == 0), "MN-major B tile");
+    static constexpr int kBAtomBytes = 64 * kBlockK * 2;  // one 64-column x 64-K-row MN-major atom column
     static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
 
@@ -146,12 +149,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
            (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
-// tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
-// fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in
-// bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
+// Descriptor for an MN-major operand tile written by TMA as 64-element-wide
+// (128-byte) columns of 64 K rows each, 128-byte swizzled: the leading byte
+// offset is the distance between consecutive 64-element MN atoms (one
+// 64 x 64 box, 8 KB), the stride byte offset the distance between groups of
+// 8 K rows (1024 bytes); other fields as for the K-major form.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr)
 {
-    return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+    return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(8192 >> 4) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+// fp16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B K-major (bit 16 = 0)
+// or MN-major (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major = false)
+{
+    return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // Bounded wait on phase `parity` of the barrier at `bar`.
@@ -211,10 +225,10 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int CG, int BN, int STAGES, int MC>
+template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = KernelCfg<CG, BN, STAGES, MC>;
+    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16>;
     constexpr int CS = Cfg::kCS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -291,7 +305,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                         const uint32_t a_dst = base + Cfg::kOffA + stage * Cfg::kABytes;
                         const uint32_t b_dst = base + Cfg::kOffB + stage * Cfg::kBBytes;
                         const int32_t k0 = int32_t(kb * kBlockK);
-                        if constexpr (CG == 1) {
+                        if constexpr (!B_KMAJOR) {
+                            // B stored [K, N]: 64-column boxes of 64 K rows (tensor coordinates {n, k})
+                            const uint32_t fbl = (CG == 1) ? fb : ptx::map_to_rank(fb, pair_leader);
+                            if (leader) ptx::mbar_arrive_expect_tx(fb, Cfg::kStageTx);
+                            if constexpr (CG == 1) ptx::tma_load_2d(a_dst, &p.tmap_a, fbl, k0, m0);
+                            else ptx::tma_load_2d_pair(a_dst, &p.tmap_a, fbl, k0, m0);
+#pragma unroll
+                            for (int h = 0; h < Cfg::kBNCta / 64; ++h) {
+                                if constexpr (CG == 1)
+                                    ptx::tma_load_2d(b_dst + h * Cfg::kBAtomBytes, &p.tmap_b, fbl, n0 + 64 * h, k0);
+                                else
+                                    ptx::tma_load_2d_pair(b_dst + h * Cfg::kBAtomBytes, &p.tmap_b, fbl, n0 + 64 * h, k0);
+                            }
+                        } else if constexpr (CG == 1) {
                             ptx::mbar_arrive_expect_tx(fb, Cfg::kStageTx);
                             ptx::tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
                             ptx::tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
@@ -318,7 +345,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (leader && lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(Cfg::kBM, BN);
+            constexpr uint32_t idesc = idesc_f16_f32(Cfg::kBM, BN, !B_KMAJOR);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             for_each_segment(p, cluster_id, num_clusters, [&](uint32_t, uint32_t k_lo, uint32_t k_hi) {
                 if (!wait_bounded<CG>(bar_acc_empty(acc), acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty))
@@ -329,11 +356,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     if (!wait_bounded<CG>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
                     ptx::tc_fence_after_sync();
                     const uint64_t a_desc = smem_desc_sw128(base + Cfg::kOffA + stage * Cfg::kABytes);
-                    const uint64_t b_desc = smem_desc_sw128(base + Cfg::kOffB + stage * Cfg::kBBytes);
+                    const uint32_t b_addr = base + Cfg::kOffB + stage * Cfg::kBBytes;
+                    const uint64_t b_desc = B_KMAJOR ? smem_desc_sw128(b_addr) : smem_desc_sw128_mn(b_addr);
+                    // per 16-element K step: +32 bytes inside a K-major swizzle atom; +2048 bytes
+                    // (two 8-row groups) in an MN-major tile
+                    constexpr uint64_t kBStep = B_KMAJOR ? 2u : (2048u >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
-                        // +32 bytes along K inside the swizzle atom per 16-element step
-                        ptx::mma_f16<CG>(d_tmem, a_desc + uint64_t(2 * kk), b_desc + uint64_t(2 * kk), idesc,
+                        ptx::mma_f16<CG>(d_tmem, a_desc + uint64_t(2 * kk), b_desc + kBStep * uint64_t(kk), idesc,
                                          (kb != k_lo || kk != 0) ? 1u : 0u);
                     }
                     // the stage is free in every CTA whose producer writes into this pair's stage
@@ -456,6 +486,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                                 r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
                                 r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
                             }
+                        }
+                        if constexpr (!C_F16) {
+                            // fp32 result: 32-column (128-byte) swizzled boxes
+#pragma unroll
+                            for (int h = 0; h < W / 32; ++h) {
+                                if (col + 32u * h >= p.n) break;
+                                const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
+                                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                                __syncwarp();
+                                const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), r[32 * h + 4 * j],
+                                                      r[32 * h + 4 * j + 1], r[32 * h + 4 * j + 2],
+                                                      r[32 * h + 4 * j + 3]);
+                                ptx::fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    ptx::tma_store_2d(&p.tmap_c, buf, int32_t(col + 32u * h), int32_t(row0));
+                                    ptx::bulk_commit_group();
+                                }
+                                ++stores;
+                            }
+                            return;
                         }
                         const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
                         if (lane == 0) ptx::bulk_wait_group_read<1>();  // this buffer's previous store has read it

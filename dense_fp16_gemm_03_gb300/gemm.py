@@ -44,6 +44,7 @@ class Plan(ctypes.Structure):
         ("stages", ctypes.c_int32),
         ("raster_width", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
         ("m", ctypes.c_int64),
         ("n", ctypes.c_int64),
         ("k", ctypes.c_int64),
@@ -74,6 +75,7 @@ EXPORTED = [
     "gemm_f16_nt", "gemm_f16_nt_ws", "gemm_f16_nt_run", "gemm_f16_nt_host",
     "gemm_f16_take_device_error", "gemm_f16_raster_coord", "gemm_f16_fast_divmod",
     "gemm_f16_nt_run_stall_test", "gemm_f16_nt_noalloc",
+    "gemm_f16_nn_f32", "gemm_f16_nn_f32_ws", "gemm_f16_nn_f32_plan_ex",
 ]
 
 _lib = None
@@ -93,7 +95,7 @@ def lib():
     sig = {
         "gemm_f16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "gemm_f16_variant_count": (i32, []),
-        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32]),
+        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32]),
         "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),
         "gemm_f16_nt_plan_for": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, P]),
         "gemm_f16_nt_plan_ex": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, P]),
@@ -107,6 +109,9 @@ def lib():
         "gemm_f16_fast_divmod": (ctypes.c_int, [u32, u32, pu32, pu32]),
         "gemm_f16_nt_run_stall_test": (ctypes.c_int, [P, vp, vp, vp, u32, ctypes.c_longlong, vp]),
         "gemm_f16_nt_noalloc": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp]),
+        "gemm_f16_nn_f32": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp]),
+        "gemm_f16_nn_f32_ws": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
+        "gemm_f16_nn_f32_plan_ex": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -149,10 +154,11 @@ def gemm_f16_variant_count():
 
 
 def gemm_f16_variant_info(variant):
-    cg, bn, st, sm = (ctypes.c_int32() for _ in range(4))
+    cg, bn, st, sm, cl, lay = (ctypes.c_int32() for _ in range(6))
     _check(lib().gemm_f16_variant_info(variant, ctypes.byref(cg), ctypes.byref(bn), ctypes.byref(st),
-                                       ctypes.byref(sm)), "gemm_f16_variant_info")
-    return {"cta_group": cg.value, "block_n": bn.value, "stages": st.value, "smem_bytes": sm.value}
+                                       ctypes.byref(sm), ctypes.byref(cl), ctypes.byref(lay)), "gemm_f16_variant_info")
+    return {"cta_group": cg.value, "block_n": bn.value, "stages": st.value, "smem_bytes": sm.value,
+            "cluster": cl.value, "layout": lay.value}
 
 
 def gemm_f16_nt_plan(m, n, k):
@@ -242,6 +248,43 @@ def gemm_f16_nt_noalloc(a, b, c, stream=None):
         raise ValueError("c must be a contiguous float16 [M,N] tensor")
     _check(lib().gemm_f16_nt_noalloc(m, n, k, _ptr(a), _ptr(b), _ptr(c), _stream(stream)), "gemm_f16_nt_noalloc")
     return c
+
+
+def _shape_kn(a, b_kn):
+    if a.dim() != 2 or b_kn.dim() != 2 or a.shape[1] != b_kn.shape[0]:
+        raise ValueError("a must be [M,K] and b [K,N]")
+    import torch
+    for t in (a, b_kn):
+        if t.dtype != torch.float16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("operands must be contiguous float16 CUDA tensors")
+    return a.shape[0], b_kn.shape[1], a.shape[1]
+
+
+def gemm_f16_nn_f32(a, b_kn, d=None, stream=None):
+    """D = A . B for fp16 A [M,K] and B [K,N] (both row-major); D [M,N] float32."""
+    import torch
+    m, n, k = _shape_kn(a, b_kn)
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.float32, device=a.device)
+    elif tuple(d.shape) != (m, n) or d.dtype != torch.float32 or not d.is_contiguous():
+        raise ValueError("d must be a contiguous float32 [M,N] tensor")
+    _check(lib().gemm_f16_nn_f32(m, n, k, _ptr(a), _ptr(b_kn), _ptr(d), _stream(stream)), "gemm_f16_nn_f32")
+    return d
+
+
+def gemm_f16_nn_f32_ws(a, b_kn, d, workspace, stream=None):
+    m, n, k = _shape_kn(a, b_kn)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().gemm_f16_nn_f32_ws(m, n, k, _ptr(a), _ptr(b_kn), _ptr(d), _ptr(workspace), ws_bytes,
+                                    _stream(stream)), "gemm_f16_nn_f32_ws")
+    return d
+
+
+def gemm_f16_nn_f32_plan_ex(m, n, k, variant=-1, raster_width=0, stream_k=-1):
+    p = Plan()
+    _check(lib().gemm_f16_nn_f32_plan_ex(m, n, k, variant, raster_width, stream_k, ctypes.byref(p)),
+           "gemm_f16_nn_f32_plan_ex")
+    return p
 
 
 def gemm_f16_nt_host(a_host, b_host, c_host, a_dev, b_dev, c_dev, workspace=None, stream=None):

@@ -80,6 +80,7 @@ typedef struct gemm_f16_plan {
     int32_t stages;          /* shared-memory ring depth */
     int32_t raster_width;    /* N-columns per raster group (>= 1) */
     int32_t stream_k;        /* 0: every tile data-parallel; 1: data-parallel waves + stream-K tail */
+    int32_t layout;          /* 0: B [N,K] and fp16 C (gemm_f16_nt*); 1: B [K,N] and fp32 D (gemm_f16_nn_f32*) */
     int64_t m, n, k;
     int64_t tiles_m, tiles_n, num_tiles;
     int64_t k_blocks;        /* ceil(k / block_k) */
@@ -112,7 +113,8 @@ const char *gemm_f16_status_string(gemm_status_t status);
  * Returns GEMM_ERR_INVALID_ARG for an index out of range. */
 int32_t gemm_f16_variant_count(void);
 gemm_status_t gemm_f16_variant_info(int32_t variant, int32_t *cta_group, int32_t *block_n,
-                                    int32_t *stages, int32_t *smem_bytes);
+                                    int32_t *stages, int32_t *smem_bytes, int32_t *cluster,
+                                    int32_t *layout);
 
 /*
  * Plan for the current CUDA device: validates the shape, checks the device
@@ -163,8 +165,9 @@ gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const 
 gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
                              void *c, void *workspace, size_t ws_bytes, gemm_stream_t stream);
 
-/* Launch a given plan (from gemm_f16_nt_plan or gemm_f16_nt_plan_for, made
- * for the current device's SM count).  The plan is re-validated. */
+/* Launch a given plan (from any plan query, made for the current device's
+ * SM count; either layout, c then being the plan's C or D).  The plan is
+ * re-validated. */
 gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c,
                               void *workspace, size_t ws_bytes, gemm_stream_t stream);
 
@@ -179,6 +182,28 @@ gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const 
 gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_host,
                                const void *b_host, void *c_host, void *a_dev, void *b_dev,
                                void *c_dev, void *workspace, size_t ws_bytes, gemm_stream_t stream);
+
+/*
+ * The layout of "wgmma_gemm.cu" (its kernel and its CPU reference gemmCpu):
+ *
+ *     D[M,N] = A[M,K] . B[K,N]      fp16 operands, fp32 accumulation, fp32 result
+ *
+ * a: device pointer to M*K fp16, row-major (K contiguous); b: device pointer
+ * to K*N fp16, row-major (N contiguous, i.e. B is not transposed); d: device
+ * pointer to M*N fp32, row-major, fully overwritten with the fp32
+ * accumulator (no rounding to fp16).  Same validation, errors, ownership and
+ * asynchrony as gemm_f16_nt (k % 8 == 0, n % 8 == 0, 16-byte aligned
+ * pointers); gemm_f16_nn_f32 uses a plan that needs no workspace,
+ * gemm_f16_nn_f32_ws may add a stream-K tail (size from the workspace_bytes
+ * of gemm_f16_nn_f32_plan_ex(m, n, k, -1, 0, -1, ...)).  Plans of this layout
+ * also run through gemm_f16_nt_run.
+ */
+gemm_status_t gemm_f16_nn_f32(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
+                              void *d, gemm_stream_t stream);
+gemm_status_t gemm_f16_nn_f32_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
+                                 void *d, void *workspace, size_t ws_bytes, gemm_stream_t stream);
+gemm_status_t gemm_f16_nn_f32_plan_ex(int64_t m, int64_t n, int64_t k, int32_t variant,
+                                      int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out);
 
 /*
  * Reads and clears the current device's error word after synchronizing

@@ -56,6 +56,7 @@ def test_variant_table(L):
         assert info["cta_group"] in (1, 2)
         assert info["block_n"] % 32 == 0 and 64 <= info["block_n"] <= 256
         assert info["smem_bytes"] <= 232448
+        assert info["layout"] in (0, 1) and info["cluster"] in (1, 2, 4)
     with pytest.raises(G.GemmError):
         G.gemm_f16_variant_info(n)
 
@@ -129,6 +130,7 @@ def test_plan_for_shapes(L):
 def test_plan_rejects_bad_shapes(L, m, n, k, status):
     p = G.Plan()
     assert L.gemm_f16_nt_plan_for(m, n, k, 148, 0, -1, 0, 0, ctypes.byref(p)) == status
+    assert L.gemm_f16_nn_f32(m, n, k, 1 << 20, 1 << 20, 1 << 20, None) == status
 
 
 def test_argument_errors_before_any_device_call(L):
@@ -219,3 +221,18 @@ def test_stream_k_covers_every_k_block_once(L, shape):
         assert len(cover) == p.num_tiles * p.k_blocks
         for t, w in owners.items():                                   # contributors come after the owner
             assert all(cover[(t, kb)] >= w for kb in range(p.k_blocks))
+
+
+def test_layout_of_plans(L):
+    for v in range(G.gemm_f16_variant_count()):
+        info = G.gemm_f16_variant_info(v)
+        p = G.gemm_f16_nt_plan_for(1000, 1000, 1000, 152, 0, v, 0, 0)
+        assert p.layout == info["layout"] and p.cluster == info["cluster"]
+    assert G.gemm_f16_nt_plan_for(8192, 8192, 8192, 152).layout == 0     # automatic plans are NT
+
+
+def test_nn_argument_errors(L):
+    good = 1 << 20
+    assert L.gemm_f16_nn_f32(8, 8, 8, None, good, good, None) == G.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_nn_f32(8, 8, 8, good, good, good + 4, None) == G.GEMM_ERR_ALIGNMENT
+    assert L.gemm_f16_nn_f32(0, 8, 8, None, None, None, None) == G.GEMM_OK

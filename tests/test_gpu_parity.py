@@ -25,7 +25,8 @@ def _gpu():
 
 
 def _variants():
-    return list(range(G.gemm_f16_variant_count()))
+    """The compiled variants of this layout (B [N,K], fp16 C)."""
+    return [v for v in range(G.gemm_f16_variant_count()) if G.gemm_f16_variant_info(v)["layout"] == 0]
 
 
 # ------------------------------------------------------------------ small
