@@ -209,6 +209,76 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+# Pipeline ablation on GB300, rung by rung, after the Hopper tutorial's
+# version table ("1. WGMMA" section "Performance"; "4. Pipeline Abstraction
+# and Two Consumer Warp Groups" sections "Pipeline Depth" and "Performance"):
+# (label, page analogue, variant, raster width, one tile per cluster?)
+ABLATION = [
+    ("single stage: TMA load, then MMA, then the next load", "V1", 8, 1, True),
+    ("two-stage ring, TMA producer warp", "V3", 9, 1, True),
+    ("CTA pair (two accumulators share B), three stages", "V4", 10, 1, True),
+    ("CTA pair, six stages", "-", 2, 1, True),
+    ("persistent: epilogue overlaps the next tile, raster 8", "-", 2, 8, False),
+    ("persistent, two pairs share B by multicast", "-", 4, 8, False),
+]
+
+
+def run_ablation(args, w):
+    import torch
+    from dense_fp16_gemm_03_gb300 import gemm as G
+
+    dev = torch.device("cuda", 0)
+    A, B = inputs.workload_operands(w)
+    a = torch.from_numpy(A.view(np.int16)).view(torch.float16).to(dev)
+    b = torch.from_numpy(B.view(np.int16)).view(torch.float16).to(dev)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    rungs = []
+    for label, page, variant, raster, one_tile in ABLATION:
+        plan = G.gemm_f16_nt_plan_ex(w.M, w.N, w.K, variant, raster, 0)
+        if one_tile:
+            plan.grid = int(plan.num_tiles * plan.cluster)
+        rungs.append((label, page, variant, raster, one_tile, plan))
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _, _, _, _, _, plan in rungs:
+        for _ in range(args.warmup):
+            G.gemm_f16_nt_run(plan, a, b, c)
+    torch.cuda.synchronize()
+    times = {i: [] for i in range(len(rungs))}
+    windows = {i: [] for i in range(len(rungs))}
+    for _ in range(max(1, args.rounds)):
+        for i, (_, _, _, _, _, plan) in enumerate(rungs):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            t0 = time.time()
+            e0.record()
+            for _ in range(args.steps):
+                G.gemm_f16_nt_run(plan, a, b, c)
+            e1.record()
+            torch.cuda.synchronize()
+            windows[i].append((t0, time.time()))
+            times[i].append(e0.elapsed_time(e1) / args.steps)
+    st, code = G.gemm_f16_take_device_error()
+    if st != G.GEMM_OK:
+        raise RuntimeError("kernel reported error word 0x%x" % code)
+    sampler.mark_begin()
+    sampler.mark_end()
+    sampler.stop()
+    for i, (label, page, variant, raster, one_tile, plan) in enumerate(rungs):
+        ms = statistics.median(times[i])
+        mhz = [float(smp[2]) for (t, smp) in sampler.samples if len(smp) > 2 and
+               any(t0 + 0.05 <= t <= t1 for (t0, t1) in windows[i])]
+        mhz_med = statistics.median(mhz) if mhz else None
+        tf = w.flops / (ms * 1e-3) / 1e12
+        print(json.dumps({"ablation_rung": i + 1, "what": label, "page_analogue": page, "variant": variant,
+                          "cta_group": plan.cta_group, "cluster": plan.cluster, "stages": plan.stages,
+                          "tile": "%dx%d" % (plan.block_m, plan.block_n), "one_tile_per_cluster": one_tile,
+                          "grid": plan.grid, "raster_width": raster, "workload": w.name, "ms": ms, "tflops": tf,
+                          "sm_mhz": mhz_med, "tflops_per_ghz": (tf / mhz_med * 1000.0) if mhz_med else None}),
+              flush=True)
+    return 0
+
+
 def workload_config(w):
     return {
         "workload": "%s: C[%d,%d] = A[%d,%d] . B[%d,%d]^T fp16, %s operands, seed %d" % (
@@ -232,6 +302,9 @@ def main():
     ap.add_argument("--variant", type=int, default=-1, help="force a compiled kernel variant (measurement)")
     ap.add_argument("--raster", type=int, default=0, help="force a raster width (measurement)")
     ap.add_argument("--stream-k", type=int, default=-1, help="force stream-K off (0) or on (1) (measurement)")
+    ap.add_argument("--ablation", action="store_true",
+                    help="time the pipeline ablation ladder (one JSON line per rung) instead of the bench step")
+    ap.add_argument("--rounds", type=int, default=3, help="interleaved rounds of the ablation ladder")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -239,6 +312,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
+    if args.ablation:
+        return run_ablation(args, w)
 
     import torch
     from dense_fp16_gemm_03_gb300 import gemm as G

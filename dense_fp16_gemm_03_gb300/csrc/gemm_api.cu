@@ -79,6 +79,10 @@ const Variant kVariants[] = {
     // B stored [K, N] (MN-major operand), fp32 result
     GEMM_VARIANT_L(1, 128, 6, 1, false, false),  // 6: 128 x 128 tile, one CTA
     GEMM_VARIANT_L(2, 256, 6, 1, false, false),  // 7: 256 x 256 tile on a CTA pair
+    // shallow rings, for the pipeline-depth ablation only
+    GEMM_VARIANT(1, 128, 1, 1),  // 8: single stage: load, then compute, then load
+    GEMM_VARIANT(1, 128, 2, 1),  // 9: two stages
+    GEMM_VARIANT(2, 256, 3, 1),  // 10: CTA pair, three stages
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
