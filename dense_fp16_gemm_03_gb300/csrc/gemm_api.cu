@@ -32,19 +32,20 @@ constexpr int kMaxDevices = 64;
 struct Variant {
     int cg, bn, stages, mc;
     int layout;  // 0: B [N,K], fp16 C; 1: B [K,N], fp32 D
+    int swap;    // 1: computes C^T = B . A^T (operands swapped, tiles stored transposed)
     int smem;
     const void *fn;
     cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
 };
 
-template <int CG, int BN, int ST, int MC, bool BK, bool CF>
+template <int CG, int BN, int ST, int MC, bool BK, bool CF, bool CT>
 cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(unsigned(plan.grid), 1, 1);
     cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC, BK, CF>::kSmemBytes);
+    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC, BK, CF, CT>::kSmemBytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     int na = 0;
@@ -57,16 +58,17 @@ cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &para
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF>, params);
+    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT>, params);
 }
 
-#define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF)                                                              \
+#define GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, CT)                                                          \
     Variant                                                                                                 \
     {                                                                                                       \
-        CG, BN, ST, MC, (BK ? 0 : 1), KernelCfg<CG, BN, ST, MC, BK, CF>::kSmemBytes,                        \
-            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF>),                    \
-            &launch_variant<CG, BN, ST, MC, BK, CF>                                                         \
+        CG, BN, ST, MC, (BK ? 0 : 1), (CT ? 1 : 0), KernelCfg<CG, BN, ST, MC, BK, CF, CT>::kSmemBytes,      \
+            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT>),                \
+            &launch_variant<CG, BN, ST, MC, BK, CF, CT>                                                     \
     }
+#define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF) GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, false)
 #define GEMM_VARIANT(CG, BN, ST, MC) GEMM_VARIANT_L(CG, BN, ST, MC, true, true)
 
 const Variant kVariants[] = {
@@ -83,6 +85,11 @@ const Variant kVariants[] = {
     GEMM_VARIANT(1, 128, 1, 1),  // 8: single stage: load, then compute, then load
     GEMM_VARIANT(1, 128, 2, 1),  // 9: two stages
     GEMM_VARIANT(2, 256, 3, 1),  // 10: CTA pair, three stages
+    GEMM_VARIANT(1, 128, 6, 2),  // 11: two CTAs along N share A by multicast (128 x 256 per cluster)
+    GEMM_VARIANT(1, 128, 6, 4),  // 12: four CTAs along N share A by multicast (128 x 512 per cluster)
+    // operands swapped (C^T = B . A^T, tiles stored transposed), for few rows of A
+    GEMM_VARIANT_X(2, 128, 8, 1, true, true, true),  // 13: B rows on the pair's M = 256, A rows on N = 128
+    GEMM_VARIANT_X(1, 128, 6, 1, true, true, true),  // 14: one CTA, 128 B rows x 128 A rows
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -251,6 +258,15 @@ int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
 // than about 86% of the slots are busy over the waves (ragged 3000x5000),
 // and loses above that, because under the power cap keeping the idle SMs of
 // a nearly full last wave busy costs clock for the whole launch.
+// Rotating the K walk of whole tiles pays when no operand strip is shared by
+// two tiles (a single row or column of tiles, e.g. 128 x 16384 x 16384:
+// measured +10%); when strips are shared, tiles that read them in K
+// lockstep hit L2 instead of DRAM, and rotation loses (8192^3: -6%).
+bool rotate_pays(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks)
+{
+    return (tiles_m == 1 || tiles_n == 1) && k_blocks >= 8;
+}
+
 bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
 {
     if (k_blocks < 4 || num_tiles * k_blocks < 2 * slots) return false;
@@ -276,16 +292,17 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     memset(&p, 0, sizeof(p));
     p.variant = variant;
     p.cta_group = var.cg;
-    p.block_m = 128 * cs;
-    p.block_n = var.bn;
+    p.block_m = 128 * var.cg * (var.cg == 2 ? var.mc : 1);  // rows per cluster tile
+    p.block_n = var.bn * (var.cg == 1 ? var.mc : 1);      // columns per cluster tile
     p.block_k = kBlockK;
     p.stages = var.stages;
     p.layout = var.layout;
     p.m = m;
     p.n = n;
     p.k = k;
-    p.tiles_m = cdiv(m, p.block_m);
-    p.tiles_n = cdiv(n, p.block_n);
+    // a swapped variant tiles the transposed problem: B's n rows on the MMA's M side
+    p.tiles_m = cdiv(var.swap ? n : m, p.block_m);
+    p.tiles_n = cdiv(var.swap ? m : n, p.block_n);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = cdiv(k, kBlockK);
     p.cluster = cs;
@@ -299,7 +316,10 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.dp_tiles = p.num_tiles;
     p.sk_iters = 0;
     p.workspace_bytes = 0;
-    const bool want_sk = stream_k == 1 || (stream_k < 0 && streamk_pays(p.num_tiles, p.k_blocks, slots));
+    p.k_rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks) ? 1 : 0;
+    // the stream-K tail would not rotate: keep whole rotated tiles where rotation pays
+    const bool want_sk = stream_k == 1 ||
+                         (stream_k < 0 && !p.k_rotate && streamk_pays(p.num_tiles, p.k_blocks, slots));
     if (want_sk && p.num_tiles > 0) {
         // whole waves but the last one or two stay data-parallel; the rest is split evenly
         const int64_t full_waves = p.num_tiles / slots;
@@ -391,6 +411,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         plan.grid < plan.cluster || plan.grid % plan.cluster != 0)
         return GEMM_ERR_INVALID_ARG;
     const int64_t workers = plan.grid / plan.cluster;
+    if (plan.k_rotate != 0 && plan.k_rotate != 1) return GEMM_ERR_INVALID_ARG;
     if (plan.stream_k == 0) {
         // any grid of whole clusters is correct: the kernel walks the tiles persistently
         if (plan.dp_tiles != plan.num_tiles || plan.sk_iters != 0 || workers > plan.num_tiles)
@@ -400,7 +421,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         if (plan.stream_k != 1 || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
             plan.sk_iters != (plan.num_tiles - plan.dp_tiles) * plan.k_blocks || plan.sk_iters < workers ||
             workers > dev->max_clusters[plan.variant] ||
-            int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, plan.block_n))
+            int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, kVariants[plan.variant].bn))
             return GEMM_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
     }
@@ -411,13 +432,22 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     if (st != GEMM_OK) return st;
     KernelParams params;
     memset(&params, 0, sizeof(params));
-    st = encode_matrix(enc, &params.tmap_a, a, uint64_t(plan.m), uint64_t(plan.k), kBlockK, 128);
+    // kernel-side problem: the transposed one for a swapped variant
+    const void *ka = var.swap ? b : a;
+    const void *kb = var.swap ? a : b;
+    const int64_t km = var.swap ? plan.n : plan.m;
+    const int64_t kn = var.swap ? plan.m : plan.n;
+    st = encode_matrix(enc, &params.tmap_a, ka, uint64_t(km), uint64_t(plan.k), kBlockK,
+                       uint32_t((var.cg == 1 && var.mc > 1) ? 128 / var.mc : 128));
     if (st != GEMM_OK) return st;
     if (var.layout == 0) {
-        st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.n), uint64_t(plan.k), kBlockK,
-                           uint32_t(var.bn / var.cg / var.mc));
+        st = encode_matrix(enc, &params.tmap_b, kb, uint64_t(kn), uint64_t(plan.k), kBlockK,
+                           uint32_t(var.bn / var.cg / (var.cg == 2 ? var.mc : 1)));
         if (st != GEMM_OK) return st;
-        st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
+        if (var.swap)  // C [m, n] written in transposed tiles: boxes of 32 columns x 64 rows, unswizzled
+            st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, 64, false);
+        else
+            st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
     } else {
         // B [K, N]: 64-column boxes of 64 K rows; D [M, N] fp32: 32-column boxes
         st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.k), uint64_t(plan.n), 64, kBlockK);
@@ -430,17 +460,18 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         if (st != GEMM_OK) return st;
     }
     params.raster = make_raster(uint32_t(plan.tiles_m), uint32_t(plan.tiles_n), uint32_t(plan.raster_width));
-    params.m = uint32_t(plan.m);
-    params.n = uint32_t(plan.n);
+    params.m = uint32_t(km);
+    params.n = uint32_t(kn);
     params.k = uint32_t(plan.k);
     params.num_tiles = uint32_t(plan.num_tiles);
     params.k_blocks = uint32_t(plan.k_blocks);
     params.dp_tiles = uint32_t(plan.dp_tiles);
+    params.k_rotate = plan.k_rotate ? 1u : 0u;
     params.sk_iters = uint64_t(plan.sk_iters);
     if (plan.stream_k) {
         params.partials = static_cast<float *>(ws);
         params.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) +
-                                                    streamk_partials_bytes(plan.grid, plan.block_n));
+                                                    streamk_partials_bytes(plan.grid, var.bn));
         if (cudaMemsetAsync(params.flags, 0, size_t(plan.grid) * 4u, stream) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
@@ -494,9 +525,10 @@ int32_t gemm_f16_variant_count(void)
 }
 
 gemm_status_t gemm_f16_variant_info(int32_t v, int32_t *cta_group, int32_t *block_n, int32_t *stages,
-                                    int32_t *smem_bytes, int32_t *cluster, int32_t *layout)
+                                    int32_t *smem_bytes, int32_t *cluster, int32_t *layout, int32_t *swapped)
 {
     if (v < 0 || v >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+    if (swapped) *swapped = kVariants[v].swap;
     if (cluster) *cluster = kVariants[v].cg * kVariants[v].mc;
     if (layout) *layout = kVariants[v].layout;
     if (cta_group) *cta_group = kVariants[v].cg;

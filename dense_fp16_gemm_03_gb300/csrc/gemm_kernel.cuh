@@ -27,7 +27,11 @@
 // CTA of the pair issues the MMA for both, and each CTA's tensor memory
 // holds its own 128 output rows.
 //
-// MC > 1 (with CG == 2) stacks MC CTA pairs along M in one cluster: the
+// MC > 1 with CG == 1 puts MC single CTAs side by side along N in one
+// cluster: they need the same A rows, so each loads 1/MC of the A tile and
+// multicasts it to all of them (A + B per CTA becomes A/MC + B).
+//
+// MC > 1 with CG == 2 stacks MC CTA pairs along M in one cluster: the
 // pairs work on vertically adjacent tiles that need the same B columns, so
 // each CTA loads only 1/MC of its half of the B tile and multicasts it to
 // the CTAs with the same rank-in-pair of the other pairs; a ring stage is
@@ -93,6 +97,7 @@ struct KernelParams {
     uint32_t num_tiles;
     uint32_t k_blocks;
     uint32_t dp_tiles;    // tiles [0, dp_tiles) are walked data-parallel
+    uint32_t k_rotate;    // 1: a whole tile starts its K walk at a per-tile offset (see the producer)
     uint64_t sk_iters;    // K iterations of tiles [dp_tiles, num_tiles), split evenly over the clusters
     float *partials;      // stream-K workspace: one 128 x BN fp32 partial tile per CTA
     uint32_t *flags;      // stream-K workspace: one "partial published" flag per CTA, zero at launch
@@ -102,18 +107,21 @@ struct KernelParams {
     uint32_t *error_word;
 };
 
-template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true>
+template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true, bool C_TRANS = false>
 struct KernelCfg {
     static_assert(CG == 1 || CG == 2, "cta group");
-    static_assert(MC == 1 || (CG == 2 && (MC == 2 || MC == 4)), "B multicast needs CTA pairs");
+    static_assert(MC == 1 || MC == 2 || MC == 4, "cluster multicast width");
+    static constexpr bool kAMC = (CG == 1 && MC > 1);  // single CTAs along N share A by multicast
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile N");
     static constexpr int kFullChunks = BN / 64;      // 64-column epilogue chunks
     static constexpr bool kTail = (BN % 64) != 0;   // plus one 32-column chunk
     static constexpr int kCS = CG * MC;             // CTAs per cluster
     static constexpr int kBM = 128 * CG;            // MMA M (one pair)
-    static constexpr int kBMCluster = kBM * MC;     // output rows per scheduling unit
-    static constexpr int kBNCta = BN / CG;          // B rows in one CTA's ring stage
-    static constexpr int kBSlice = kBNCta / MC;     // B rows one CTA loads per stage
+    static constexpr int kBMCluster = kAMC ? kBM : kBM * MC;  // output rows per scheduling unit
+    static constexpr int kBNCluster = kAMC ? BN * MC : BN;    // output columns per scheduling unit
+    static constexpr int kBNCta = BN / CG;                    // B rows in one CTA's ring stage
+    static constexpr int kBSlice = kAMC ? kBNCta : kBNCta / MC;  // B rows one CTA loads per stage
+    static constexpr int kASlice = kAMC ? 128 / MC : 128;        // A rows one CTA loads per stage
     static constexpr int kABytes = 128 * kBlockK * 2;
     static constexpr int kBBytes = kBNCta * kBlockK * 2;
     static constexpr int kStageTx = (kABytes + kBBytes) * CG;  // bytes landing on one full barrier
@@ -128,7 +136,12 @@ struct KernelCfg {
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kAccCols = (BN + 63) / 64 * 64;  // accumulator buffer stride (64-column aligned)
     static constexpr int kTmemCols = (2 * kAccCols <= 128) ? 128 : (2 * kAccCols <= 256 ? 256 : 512);
-    static_assert(kBBytes % 1024 == 0 && kABytes % 1024 == 0 && (kBSlice * 128) % 1024 == 0, "swizzle atoms");
+    static_assert(kBBytes % 1024 == 0 && kABytes % 1024 == 0 && (kBSlice * 128) % 1024 == 0 &&
+                      (kASlice * 128) % 1024 == 0, "swizzle atoms");
+    static_assert(!kAMC || B_KMAJOR, "A multicast with K-major B only");
+    // C_TRANS: the kernel computes the transposed product (operands swapped by the host) and
+    // the epilogue writes each tile transposed
+    static_assert(!C_TRANS || (C_F16 && B_KMAJOR && BN % 64 == 0), "transposed store: fp16, K-major");
     static_assert(BN % (16 * CG) == 0, "MMA N");
     // B stored [K, N] (MN-major operand): whole 64-column swizzle atoms, no multicast slices
     static_assert(B_KMAJOR || (MC == 1 && kBNCta % 64 == 0), "MN-major B tile");
@@ -168,13 +181,14 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_maj
     return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-// Bounded wait on phase `parity` of the barrier at `bar`.
-template <int CG>
+// Bounded wait on phase `parity` of the barrier at `bar` (cluster-scope
+// acquire when the cluster has more than one CTA).
+template <int CS>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const KernelParams &p,
                                              volatile uint32_t *abort_flag, uint32_t code)
 {
     auto try_once = [&]() {
-        if constexpr (CG == 2) return ptx::mbar_try_wait_cluster(bar, parity);
+        if constexpr (CS > 1) return ptx::mbar_try_wait_cluster(bar, parity);
         else return ptx::mbar_try_wait(bar, parity);
     };
     if (try_once()) return true;
@@ -225,10 +239,10 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16>
+template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16>;
+    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS>;
     constexpr int CS = Cfg::kCS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -292,10 +306,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
                 uint32_t mb, nb;
                 raster_coord(p.raster, tile, mb, nb);
-                const int32_t m0 = int32_t(mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u);
-                const int32_t n0 = int32_t(nb * BN + pair_rank * Cfg::kBNCta + pair * Cfg::kBSlice);
+                const int32_t m0 = Cfg::kAMC ? int32_t(mb * 128u + cta_rank * Cfg::kASlice)
+                                             : int32_t(mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u);
+                const int32_t n0 = Cfg::kAMC ? int32_t((nb * MC + cta_rank) * BN)
+                                             : int32_t(nb * BN + pair_rank * Cfg::kBNCta + pair * Cfg::kBSlice);
+                // With k_rotate, a whole tile walks its K blocks from a per-tile offset, wrapping
+                // around: when no operand strip is shared between tiles, lockstep K walks make every
+                // CTA read the same K column of rows a power-of-two pitch apart, which piles the
+                // requests onto the same DRAM channels.  The MMA consumes stages in order either way.
+                const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
+                const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb, ++fills) {
-                    if (!wait_bounded<CG>(bar_empty(stage), phase ^ 1u, p, abort_flag, kErrWaitEmpty)) {
+                    if (!wait_bounded<CS>(bar_empty(stage), phase ^ 1u, p, abort_flag, kErrWaitEmpty)) {
                         ok = false;
                         return false;
                     }
@@ -304,7 +326,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                         const uint32_t fb = bar_full(stage);
                         const uint32_t a_dst = base + Cfg::kOffA + stage * Cfg::kABytes;
                         const uint32_t b_dst = base + Cfg::kOffB + stage * Cfg::kBBytes;
-                        const int32_t k0 = int32_t(kb * kBlockK);
+                        uint32_t kr = kb + rot;
+                        if (kr >= p.k_blocks) kr -= p.k_blocks;
+                        const int32_t k0 = int32_t(kr * kBlockK);
                         if constexpr (!B_KMAJOR) {
                             // B stored [K, N]: 64-column boxes of 64 K rows (tensor coordinates {n, k})
                             const uint32_t fbl = (CG == 1) ? fb : ptx::map_to_rank(fb, pair_leader);
@@ -318,6 +342,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                                 else
                                     ptx::tma_load_2d_pair(b_dst + h * Cfg::kBAtomBytes, &p.tmap_b, fbl, n0 + 64 * h, k0);
                             }
+                        } else if constexpr (Cfg::kAMC) {
+                            // every CTA of the cluster receives the whole A tile, 1/MC from each
+                            ptx::mbar_arrive_expect_tx(fb, Cfg::kStageTx);
+                            ptx::tma_load_2d_mc(a_dst + cta_rank * Cfg::kASlice * 128u, &p.tmap_a, fb, k0, m0,
+                                                uint16_t((1u << CS) - 1u));
+                            ptx::tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
                         } else if constexpr (CG == 1) {
                             ptx::mbar_arrive_expect_tx(fb, Cfg::kStageTx);
                             ptx::tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
@@ -348,12 +378,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             constexpr uint32_t idesc = idesc_f16_f32(Cfg::kBM, BN, !B_KMAJOR);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             for_each_segment(p, cluster_id, num_clusters, [&](uint32_t, uint32_t k_lo, uint32_t k_hi) {
-                if (!wait_bounded<CG>(bar_acc_empty(acc), acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty))
+                if (!wait_bounded<CS>(bar_acc_empty(acc), acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty))
                     return false;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols;
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb) {
-                    if (!wait_bounded<CG>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
+                    if (!wait_bounded<CS>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
                     ptx::tc_fence_after_sync();
                     const uint64_t a_desc = smem_desc_sw128(base + Cfg::kOffA + stage * Cfg::kABytes);
                     const uint32_t b_addr = base + Cfg::kOffB + stage * Cfg::kBBytes;
@@ -367,7 +397,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                                          (kb != k_lo || kk != 0) ? 1u : 0u);
                     }
                     // the stage is free in every CTA whose producer writes into this pair's stage
-                    if constexpr (CG == 1) ptx::mma_commit(bar_empty(stage));
+                    if constexpr (Cfg::kAMC) ptx::mma_commit_mc(bar_empty(stage), uint16_t((1u << CS) - 1u));
+                    else if constexpr (CG == 1) ptx::mma_commit(bar_empty(stage));
                     else ptx::mma_commit_pair(bar_empty(stage), uint16_t((1u << CS) - 1u));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -405,9 +436,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
-            const uint32_t row0 = mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u + quarter * 32u;
-            const uint32_t col0 = nb * BN;
-            const bool ok = wait_bounded<CG>(bar_acc_full(acc), acc_phase, p, abort_flag, kErrWaitAccFull);
+            const uint32_t row0 = Cfg::kAMC ? mb * 128u + quarter * 32u
+                                            : mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u + quarter * 32u;
+            const uint32_t col0 = Cfg::kAMC ? (nb * MC + cta_rank) * BN : nb * BN;
+            const bool ok = wait_bounded<CS>(bar_acc_full(acc), acc_phase, p, abort_flag, kErrWaitAccFull);
             // A split tile meets the other epilogue warps at named barrier 1 below, so the decision
             // to stop must be the same in all four warps; a whole tile needs it per warp only.
             const bool split = (k_lo != 0) || (k_hi != p.k_blocks);
@@ -486,6 +518,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                                 r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
                                 r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
                             }
+                        }
+                        if constexpr (C_TRANS) {
+                            // The tile is D' = C^T: lane = a column n of C, register j = row m of C.
+                            // Stage a [64 m][32 n] fp16 block (64-byte rows, unswizzled), store it
+                            // with a {32 n, 64 m} box at (n = row0, m = col).
+                            const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
+                            if (lane == 0) ptx::bulk_wait_group_read<1>();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < W; ++j)
+                                ptx::st_shared_u16(buf + uint32_t(j) * 64u + lane * 2u,
+                                                   __half_as_ushort(__float2half_rn(__uint_as_float(r[j]))));
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_2d(&p.tmap_c, buf, int32_t(row0), int32_t(col));
+                                ptx::bulk_commit_group();
+                            }
+                            ++stores;
+                            return;
                         }
                         if constexpr (!C_F16) {
                             // fp32 result: 32-column (128-byte) swizzled boxes

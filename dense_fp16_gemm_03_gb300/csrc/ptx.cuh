@@ -136,6 +136,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Load multicast to every CTA in `cta_mask` of the cluster: the box lands at
+// the same shared offset in each, and its bytes complete on the barrier at
+// `bar`'s offset in each destination CTA.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                               uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
 // CTA-pair load multicast to every CTA in `cta_mask` (same shared offset in
 // each); each destination's bytes complete on the barrier at `bar`'s offset
 // in the first CTA of that destination's pair.
@@ -260,6 +273,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
                  : "memory");
 }
 
+// Single-CTA MMA, arrival multicast to the barrier at the same shared offset
+// in every CTA of `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // CTA-pair form: arrive on the barrier at the same shared offset in every
 // CTA of `cta_mask`.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
@@ -350,6 +374,11 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
 }
 
 // --------------------------------------------------------- shared memory
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)

@@ -45,6 +45,7 @@ class Plan(ctypes.Structure):
         ("raster_width", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
         ("layout", ctypes.c_int32),
+        ("k_rotate", ctypes.c_int32),
         ("m", ctypes.c_int64),
         ("n", ctypes.c_int64),
         ("k", ctypes.c_int64),
@@ -95,7 +96,7 @@ def lib():
     sig = {
         "gemm_f16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "gemm_f16_variant_count": (i32, []),
-        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32]),
+        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32, pi32]),
         "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),
         "gemm_f16_nt_plan_for": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, P]),
         "gemm_f16_nt_plan_ex": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, P]),
@@ -154,11 +155,12 @@ def gemm_f16_variant_count():
 
 
 def gemm_f16_variant_info(variant):
-    cg, bn, st, sm, cl, lay = (ctypes.c_int32() for _ in range(6))
+    cg, bn, st, sm, cl, lay, sw = (ctypes.c_int32() for _ in range(7))
     _check(lib().gemm_f16_variant_info(variant, ctypes.byref(cg), ctypes.byref(bn), ctypes.byref(st),
-                                       ctypes.byref(sm), ctypes.byref(cl), ctypes.byref(lay)), "gemm_f16_variant_info")
+                                       ctypes.byref(sm), ctypes.byref(cl), ctypes.byref(lay), ctypes.byref(sw)),
+           "gemm_f16_variant_info")
     return {"cta_group": cg.value, "block_n": bn.value, "stages": st.value, "smem_bytes": sm.value,
-            "cluster": cl.value, "layout": lay.value}
+            "cluster": cl.value, "layout": lay.value, "swapped": sw.value}
 
 
 def gemm_f16_nt_plan(m, n, k):

@@ -81,6 +81,8 @@ typedef struct gemm_f16_plan {
     int32_t raster_width;    /* N-columns per raster group (>= 1) */
     int32_t stream_k;        /* 0: every tile data-parallel; 1: data-parallel waves + stream-K tail */
     int32_t layout;          /* 0: B [N,K] and fp16 C (gemm_f16_nt*); 1: B [K,N] and fp32 D (gemm_f16_nn_f32*) */
+    int32_t k_rotate;        /* 1: whole tiles walk K from a per-tile offset (set when no operand strip is
+                                shared by two tiles; spreads DRAM requests; changes only summation order) */
     int64_t m, n, k;
     int64_t tiles_m, tiles_n, num_tiles;
     int64_t k_blocks;        /* ceil(k / block_k) */
@@ -109,12 +111,17 @@ typedef struct gemm_f16_plan {
 /* Human-readable name of a status code (static string, never NULL). */
 const char *gemm_f16_status_string(gemm_status_t status);
 
-/* Number of compiled kernel variants, and the shape of one of them.
- * Returns GEMM_ERR_INVALID_ARG for an index out of range. */
+/* Number of compiled kernel variants, and the shape of one of them: CTAs
+ * per MMA (cta_group), MMA tile N, ring depth, dynamic shared memory, CTAs
+ * per cluster, layout (as in gemm_f16_plan_t) and whether it computes the
+ * transposed product C^T = B . A^T with the operands swapped (for products
+ * with few rows of A; a plan of such a variant has tiles_m over n and
+ * tiles_n over m).  Any pointer may be NULL.  Returns GEMM_ERR_INVALID_ARG
+ * for an index out of range. */
 int32_t gemm_f16_variant_count(void);
 gemm_status_t gemm_f16_variant_info(int32_t variant, int32_t *cta_group, int32_t *block_n,
                                     int32_t *stages, int32_t *smem_bytes, int32_t *cluster,
-                                    int32_t *layout);
+                                    int32_t *layout, int32_t *swapped);
 
 /*
  * Plan for the current CUDA device: validates the shape, checks the device

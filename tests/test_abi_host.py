@@ -117,7 +117,7 @@ def test_plan_for_shapes(L):
     assert r.tiles_m == -(-3000 // r.block_m) and r.tiles_n == -(-5000 // r.block_n)
     for v in range(G.gemm_f16_variant_count()):
         q = G.gemm_f16_nt_plan_for(128, 16384, 16384, 148, variant=v, raster_width=4, stream_k=0)
-        assert q.variant == v and q.raster_width == 4
+        assert q.variant == v and q.raster_width == min(4, q.tiles_n)
         assert q.grid // q.cluster <= q.num_tiles
 
 
@@ -163,7 +163,7 @@ def test_no_cuda_device_is_an_error_not_a_crash(L):
 
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (8192, 8192, 8192),
                                    (1000, 1000, 1000), (128, 256, 8192)])
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14])
 def test_stream_k_plan_invariants(L, shape, variant):
     m, n, k = shape
     for sms in (148, 152):
@@ -173,7 +173,8 @@ def test_stream_k_plan_invariants(L, shape, variant):
             assert p.sk_iters == (p.num_tiles - p.dp_tiles) * p.k_blocks
             assert p.sk_iters >= workers and p.dp_tiles % workers == 0
             assert p.num_tiles - p.dp_tiles <= 2 * workers            # at most two waves are split
-            assert p.workspace_bytes >= p.grid * 128 * p.block_n * 4 + p.grid * 4
+            bn = G.gemm_f16_variant_info(variant)["block_n"]        # one CTA's partial tile is 128 x bn
+            assert p.workspace_bytes >= p.grid * 128 * bn * 4 + p.grid * 4
             assert workers == sms // p.cluster
         else:                                                         # too little work to split
             assert p.workspace_bytes == 0 and p.dp_tiles == p.num_tiles and p.num_tiles * p.k_blocks < workers + sms
@@ -236,3 +237,10 @@ def test_nn_argument_errors(L):
     assert L.gemm_f16_nn_f32(8, 8, 8, None, good, good, None) == G.GEMM_ERR_INVALID_ARG
     assert L.gemm_f16_nn_f32(8, 8, 8, good, good, good + 4, None) == G.GEMM_ERR_ALIGNMENT
     assert L.gemm_f16_nn_f32(0, 8, 8, None, None, None, None) == G.GEMM_OK
+
+
+def test_k_rotation_rule(L):
+    skinny = G.gemm_f16_nt_plan_for(128, 16384, 16384, 152)
+    assert skinny.k_rotate == 1 and skinny.stream_k == 0      # one row of tiles: no strip is shared
+    big = G.gemm_f16_nt_plan_for(8192, 8192, 8192, 152)
+    assert big.k_rotate == 0                                   # strips shared by neighbouring tiles

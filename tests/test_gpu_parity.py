@@ -31,7 +31,7 @@ def _variants():
 
 # ------------------------------------------------------------------ small
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14])
 def test_square_256_exact_every_variant(variant):
     w = inputs.BY_NAME["square_256"]
     A, B = inputs.workload_operands(w)
@@ -49,7 +49,7 @@ RAGGED = [(1, 8, 8), (3, 8, 16), (129, 264, 72), (128, 256, 64), (257, 136, 200)
 
 
 @pytest.mark.parametrize("shape", RAGGED)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14])
 def test_ragged_exact(shape, variant):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "eighths", seed=M + 7 * N + 13 * K)
@@ -80,7 +80,7 @@ SK_SHAPES = [(640, 1032, 520), (1000, 1000, 1000), (300, 520, 4096), (128, 256, 
 
 
 @pytest.mark.parametrize("shape", SK_SHAPES)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14])
 def test_stream_k_exact(shape, variant):
     """Split tiles are summed from fp32 partials; on integer-valued operands
     every partial and every sum is exact, so the result is still bit-exact."""
@@ -116,6 +116,22 @@ def test_workspace_entry_point_rejects_small_workspace():
     st = G.lib().gemm_f16_nt_ws(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), small.data_ptr(), need - 256,
                                 torch.cuda.current_stream().cuda_stream)
     assert st == G.GEMM_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("shape", [(128, 2048, 4096), (1000, 1000, 1000), (300, 520, 4096)])
+def test_k_rotation_exact(shape):
+    """A rotated K walk only reorders the fp32 sums: integer-valued products stay bit-exact."""
+    M, N, K = shape
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=M + 5 * N)
+    a, b = to_dev(A), to_dev(B)
+    for v in _variants():
+        plan = G.gemm_f16_nt_plan_ex(M, N, K, v, 0, 0)
+        for rot in (0, 1):
+            plan.k_rotate = rot
+            c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+            G.gemm_f16_nt_run(plan, a, b, c)
+            assert G.gemm_f16_take_device_error()[0] == G.GEMM_OK
+            assert_parity(from_dev_bits(c), A, B, exact=True)
 
 
 # ------------------------------------------------------ structured operands
