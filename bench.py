@@ -172,6 +172,21 @@ def cpu_oracle_rate(A, B, target_s=10.0):
     return 2.0 * rows * N * K / dt / 1e12, dt, rows
 
 
+def aggregate_throughput(local_ms, flops_per_step, steps, dist=None, device="cpu"):
+    """Whole-job throughput of `steps` replicated steps per rank: the slowest
+    rank's time (max over ranks) bounds the job; every rank did its own
+    steps.  Returns (TFLOP/s, max_ms).  dist: torch.distributed or None."""
+    import torch
+    world = 1
+    max_ms = float(local_ms)
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([max_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12, max_ms
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -373,12 +388,8 @@ def main():
     total_ms = starts[0].elapsed_time(ends[-1])
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_launch_ms = sum(launch_ms) / len(launch_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    value, total_ms = aggregate_throughput(total_ms, w.flops, args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
 
     # end to end through the host-buffer entry point: H2D of A and B from
     # pinned memory, the GEMM, D2H of C, every step
@@ -400,12 +411,8 @@ def main():
             G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, ws, stream=stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * w.flops * e_steps / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e_value, e_ms = aggregate_throughput(e0.elapsed_time(e1), w.flops, e_steps, dist, dev)
+        e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": 2 * (w.M * w.K + w.N * w.K), "d2h_bytes_per_step": 2 * w.M * w.N,
                "steps": e_steps}
 

@@ -19,31 +19,39 @@ from . import build as _build
 _lib = None
 
 
+def load_library(path):
+    """ctypes handle of an oracle library with its signatures declared."""
+    L = ctypes.CDLL(path)
+    _declare(L)
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        i64, u16p, f64p, i64p = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
-        L.oracle_f16_to_f64.restype = ctypes.c_double
-        L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
-        L.oracle_f64_to_f16.restype = ctypes.c_uint16
-        L.oracle_f64_to_f16.argtypes = [ctypes.c_double]
-        L.oracle_f16_to_f64_array.argtypes = [i64, u16p, f64p]
-        L.oracle_f64_to_f16_array.argtypes = [i64, f64p, u16p]
-        L.oracle_gemm_nt.restype = ctypes.c_int
-        L.oracle_gemm_nt.argtypes = [i64, i64, i64, u16p, u16p, u16p, f64p, f64p]
-        L.oracle_gemm_nt_entries.restype = ctypes.c_int
-        L.oracle_gemm_nt_entries.argtypes = [i64, i64, i64, u16p, u16p, i64, i64p, i64p, u16p, f64p, f64p]
-        L.oracle_gemm_nn_f32.restype = ctypes.c_int
-        L.oracle_gemm_nn_f32.argtypes = [i64, i64, i64, u16p, u16p, ctypes.c_void_p, f64p, f64p]
-        L.oracle_gemm_nn_f32_entries.restype = ctypes.c_int
-        L.oracle_gemm_nn_f32_entries.argtypes = [i64, i64, i64, u16p, u16p, i64, i64p, i64p, ctypes.c_void_p,
-                                                 f64p, f64p]
-        L.oracle_f64_to_f32_array.argtypes = [i64, f64p, ctypes.c_void_p]
-        L.oracle_num_threads.restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(_build.build())
     return _lib
+
+
+def _declare(L):
+    i64, u16p, f64p, i64p = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    L.oracle_f16_to_f64.restype = ctypes.c_double
+    L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+    L.oracle_f64_to_f16.restype = ctypes.c_uint16
+    L.oracle_f64_to_f16.argtypes = [ctypes.c_double]
+    L.oracle_f16_to_f64_array.argtypes = [i64, u16p, f64p]
+    L.oracle_f64_to_f16_array.argtypes = [i64, f64p, u16p]
+    L.oracle_gemm_nt.restype = ctypes.c_int
+    L.oracle_gemm_nt.argtypes = [i64, i64, i64, u16p, u16p, u16p, f64p, f64p]
+    L.oracle_gemm_nt_entries.restype = ctypes.c_int
+    L.oracle_gemm_nt_entries.argtypes = [i64, i64, i64, u16p, u16p, i64, i64p, i64p, u16p, f64p, f64p]
+    L.oracle_gemm_nn_f32.restype = ctypes.c_int
+    L.oracle_gemm_nn_f32.argtypes = [i64, i64, i64, u16p, u16p, ctypes.c_void_p, f64p, f64p]
+    L.oracle_gemm_nn_f32_entries.restype = ctypes.c_int
+    L.oracle_gemm_nn_f32_entries.argtypes = [i64, i64, i64, u16p, u16p, i64, i64p, i64p, ctypes.c_void_p,
+                                             f64p, f64p]
+    L.oracle_f64_to_f32_array.argtypes = [i64, f64p, ctypes.c_void_p]
+    L.oracle_num_threads.restype = ctypes.c_int
 
 
 def _bits(x):

@@ -14,6 +14,12 @@ LIB = os.path.join(OUT_DIR, "libgemm_oracle.so")
 FLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC", "-std=c11"]
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile an oracle source file (the real one, or a test's planted-mistake copy)."""
+    subprocess.run(["gcc", *FLAGS, "-o", out, src, "-lm"], check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
