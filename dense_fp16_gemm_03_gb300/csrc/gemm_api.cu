@@ -11,7 +11,10 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
+#include <random>
 #include <string.h>
 
 #include "gemm_f16.h"
@@ -47,15 +50,20 @@ cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &para
     cfg.blockDim = dim3(kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC, BK, CF, CT>::kSmemBytes);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int na = 0;
     if (CG * MC > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CG * MC;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        na = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = CG * MC;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    // programmatic dependent launch: the kernel's set-up may overlap the previous kernel's tail;
+    // it waits (griddepcontrol.wait) for that kernel before touching global memory
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     cfg.attrs = attr;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT>, params);
@@ -250,7 +258,26 @@ int64_t streamk_partials_bytes(int64_t grid, int32_t block_n)
 
 int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
 {
-    return streamk_partials_bytes(grid, block_n) + round_up(grid * 4, 256);
+    return streamk_partials_bytes(grid, block_n) + round_up(grid * 8, 256);
+}
+
+// Stamps of stream-K launches: a per-process random high word and a counter,
+// so a flag left by an earlier launch (or found in fresh memory) does not
+// equal the current launch's stamp; no clearing launch is needed.
+std::atomic<uint64_t> g_sk_counter{0};
+uint64_t g_sk_nonce = 0;
+std::once_flag g_sk_nonce_once;
+
+uint64_t next_sk_stamp()
+{
+    std::call_once(g_sk_nonce_once, []() {
+        std::random_device rd;
+        uint64_t r = (uint64_t(rd()) << 32) ^ uint64_t(rd()) ^
+                     uint64_t(std::chrono::steady_clock::now().time_since_epoch().count());
+        g_sk_nonce = (r & 0xFFFFFFFF00000000ull) | 0x100000000ull;  // high word, never zero
+    });
+    const uint64_t c = (g_sk_counter.fetch_add(1) + 1) & 0xFFFFFFFFull;
+    return g_sk_nonce | (c ? c : 1u);
 }
 
 // A stream-K tail pays when the data-parallel schedule would leave the last
@@ -470,12 +497,9 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     params.sk_iters = uint64_t(plan.sk_iters);
     if (plan.stream_k) {
         params.partials = static_cast<float *>(ws);
-        params.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) +
+        params.flags = reinterpret_cast<uint64_t *>(static_cast<char *>(ws) +
                                                     streamk_partials_bytes(plan.grid, var.bn));
-        if (cudaMemsetAsync(params.flags, 0, size_t(plan.grid) * 4u, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
+        params.sk_stamp = next_sk_stamp();
     }
     params.skip_fill = skip_fill;
     params.wait_limit = wait_limit;

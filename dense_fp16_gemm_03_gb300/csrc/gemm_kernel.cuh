@@ -43,7 +43,7 @@
 // the remaining tiles are cut into equal contiguous ranges, one per cluster,
 // so the last wave is not partly idle.  A cluster whose range starts inside
 // a tile publishes its fp32 partial tile to the caller's workspace and sets
-// a flag; the cluster that holds the tile's first K block adds the
+// its flag to this launch's stamp; the cluster that holds the tile's first K block adds the
 // published partials in its epilogue.  That owning segment is the last one
 // in its range while the publishing segments are the first ones in theirs,
 // so no cluster ever waits on a cluster that waits on it.
@@ -100,7 +100,8 @@ struct KernelParams {
     uint32_t k_rotate;    // 1: a whole tile starts its K walk at a per-tile offset (see the producer)
     uint64_t sk_iters;    // K iterations of tiles [dp_tiles, num_tiles), split evenly over the clusters
     float *partials;      // stream-K workspace: one 128 x BN fp32 partial tile per CTA
-    uint32_t *flags;      // stream-K workspace: one "partial published" flag per CTA, zero at launch
+    uint64_t *flags;      // stream-K workspace: one "partial published" stamp per CTA
+    uint64_t sk_stamp;    // this launch's stamp: a flag equal to it marks a partial of this launch
     uint32_t skip_fill;   // test hook: k-block fill (counted across CTA 0's tiles) the producer
                           // of CTA 0 leaves undone, to exercise the bounded waits; ~0u = none
     long long wait_limit; // cycles a single barrier wait may take before it gives up
@@ -297,6 +298,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched as a programmatic dependent: the set-up above overlaps the tail of the previous
+    // kernel in the stream; no global memory is touched before that kernel has completed.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 }
                 __threadfence();
                 ptx::named_barrier_sync(1, 32 * kEpiWarps);
-                if (first_epi_thread) ptx::st_release_gpu(p.flags + blockIdx.x, 1u);
+                if (first_epi_thread) ptx::st_release_gpu_u64(p.flags + blockIdx.x, p.sk_stamp);
             } else {
                 // ---- a whole tile, or the owning segment of a split tile
                 uint32_t first_w = 0, last_w = 0;  // contributors [first_w, last_w)
@@ -485,9 +490,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     if (first_epi_thread) {
                         for (uint32_t w = first_w; w < last_w; ++w) {
                             if (sk_begin(p, w, num_clusters) >= sk_begin(p, w + 1, num_clusters)) continue;
-                            const uint32_t *flag = p.flags + w * CS + cta_rank;
+                            const uint64_t *flag = p.flags + w * CS + cta_rank;
                             const long long t0 = clock64();
-                            while (ptx::ld_acquire_gpu(flag) == 0u) {
+                            while (ptx::ld_acquire_gpu_u64(flag) != p.sk_stamp) {
                                 if (*abort_flag || clock64() - t0 > p.wait_limit) {
                                     *abort_flag = 1u;
                                     atomicCAS(p.error_word, 0u, kErrWaitPartial | (blockIdx.x << 8));

@@ -81,6 +81,22 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// ------------------------------------------------ dependent launches
+
+// Wait until the grids this launch depends on (earlier work in the stream)
+// have completed and their memory is visible; a no-op without programmatic
+// dependent launch.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next dependent launch in the stream to be scheduled.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -350,6 +366,18 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Named barrier `id` over `count` threads (a multiple of 32).

@@ -101,9 +101,13 @@ typedef struct gemm_f16_plan {
  * contiguous ranges, one per cluster, so no cluster idles in a partial last
  * wave.  A tile split between clusters is finished by the cluster holding
  * its first K block, which adds the fp32 partial tiles the others publish in
- * the workspace.  Workspace layout: grid * block_m/cta_group * block_n fp32
- * partial tiles, then grid 32-bit flags (cleared by the library before each
- * launch).  Every cluster of the grid must be resident at once; the plan's
+ * the workspace.  Workspace layout: grid partial tiles of 128 x (the
+ * variant's MMA N) fp32 each, then grid 64-bit flags.  A flag is set to a
+ * stamp unique to the launch (a per-process random high word and a launch
+ * counter), so flags left by earlier launches or found in fresh memory never
+ * count and nothing needs clearing between launches; a workspace must not be
+ * shared by launches that overlap on the GPU.  Every cluster of the grid
+ * must be resident at once; the plan's
  * grid never exceeds that.  The fp32 partial sums change the rounding order
  * of split tiles only within the fp32 accumulation error.
  */
@@ -252,8 +256,9 @@ gemm_status_t gemm_f16_fast_divmod(uint32_t d, uint32_t n, uint32_t *q, uint32_t
  * that device current) and keeps it; make that first call before any stream
  * capture.  The call allocates nothing: no cudaMalloc, cudaFree or
  * allocating library routine.  All calls share the one array and it keeps
- * the last call's contents (the library clears the flags that must start at
- * zero before every launch), so calls whose kernels overlap on the GPU --
+ * the last call's contents (the stream-K flags in it carry per-launch stamps,
+ * so nothing there has to start at zero), so calls whose kernels overlap on
+ * the GPU --
  * two streams, or two host threads -- race on it and give wrong results;
  * serialize them.  A plan that needs more scratch than the array holds is
  * rejected with GEMM_ERR_WORKSPACE before any launch (on a 152-SM GB300 the

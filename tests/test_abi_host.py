@@ -174,7 +174,7 @@ def test_stream_k_plan_invariants(L, shape, variant):
             assert p.sk_iters >= workers and p.dp_tiles % workers == 0
             assert p.num_tiles - p.dp_tiles <= 2 * workers            # at most two waves are split
             bn = G.gemm_f16_variant_info(variant)["block_n"]        # one CTA's partial tile is 128 x bn
-            assert p.workspace_bytes >= p.grid * 128 * bn * 4 + p.grid * 4
+            assert p.workspace_bytes >= p.grid * 128 * bn * 4 + p.grid * 8
             assert workers == sms // p.cluster
         else:                                                         # too little work to split
             assert p.workspace_bytes == 0 and p.dp_tiles == p.num_tiles and p.num_tiles * p.k_blocks < workers + sms

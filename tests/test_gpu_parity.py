@@ -97,6 +97,24 @@ def test_stream_k_tolerance(shape):
         assert_parity(run_gpu(A, B, variant=v, stream_k=1), A, B)
 
 
+@pytest.mark.parametrize("fill", [0x00, 0x01, 0xFF])
+def test_stream_k_reused_and_dirty_workspace(fill):
+    """Stream-K flags carry per-launch stamps: a workspace full of leftovers or
+    of an earlier launch's flags must not let an owner read stale partials."""
+    M, N, K = 1000, 1000, 1000
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=fill + 1)
+    A2, B2 = inputs.make_operands(M, N, K, "eighths", seed=fill + 2)
+    for v in (1, 2, 4):
+        plan = G.gemm_f16_nt_plan_ex(M, N, K, v, 0, 1)
+        assert plan.stream_k == 1
+        ws = torch.full((int(plan.workspace_bytes),), fill, dtype=torch.uint8, device="cuda")
+        for (X, Y) in ((A, B), (A2, B2), (A, B)):      # back to back on one workspace
+            c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+            G.gemm_f16_nt_run(plan, to_dev(X), to_dev(Y), c, ws)
+            assert G.gemm_f16_take_device_error()[0] == G.GEMM_OK
+            assert_parity(from_dev_bits(c), X, Y, exact=True)
+
+
 def test_stream_k_plan_shape():
     sms = num_sms()
     p = G.gemm_f16_nt_plan_ex(4096, 4096, 4096, 2, 0, 1)
