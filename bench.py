@@ -366,17 +366,20 @@ def main():
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # One event pair around the K steps: events between launches would stand between two kernels
+    # in the stream and stop a launch's set-up from overlapping its predecessor's tail.  Each step
+    # is exactly one launch of the GEMM kernel, back to back, so the average launch duration is
+    # the timed region over K (inter-kernel gaps included: conservative).
+    e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.mark_begin()
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            starts[i].record(stream)
+        e_begin.record(stream)
+        for _ in range(args.steps):
             step()
-            ends[i].record(stream)
+        e_end.record(stream)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -385,9 +388,8 @@ def main():
     st, code = G.gemm_f16_take_device_error(stream)
     if st != G.GEMM_OK:
         raise RuntimeError("kernel reported error word 0x%x" % code)
-    total_ms = starts[0].elapsed_time(ends[-1])
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    total_ms = e_begin.elapsed_time(e_end)
+    mean_launch_ms = total_ms / args.steps
     value, total_ms = aggregate_throughput(total_ms, w.flops, args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
 
