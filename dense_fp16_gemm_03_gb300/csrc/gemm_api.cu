@@ -19,6 +19,7 @@
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_wide.cuh"
 
 using namespace gemm_f16;
 
@@ -39,22 +40,25 @@ struct Variant {
     int smem;
     const void *fn;
     cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
+    int threads;  // threads per CTA
+    int b_box;    // B rows per TMA box (B [N,K] layout)
 };
 
-template <int CG, int BN, int ST, int MC, bool BK, bool CF, bool CT>
-cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
+// Launch `kernel` persistently with clusters of `cs` CTAs, as a programmatic dependent launch.
+cudaError_t launch_persistent(const void *kernel, const gemm_f16_plan_t &plan, const KernelParams &params,
+                              cudaStream_t stream, int threads, int smem, int cs)
 {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(unsigned(plan.grid), 1, 1);
-    cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = size_t(KernelCfg<CG, BN, ST, MC, BK, CF, CT>::kSmemBytes);
+    cfg.blockDim = dim3(unsigned(threads), 1, 1);
+    cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (CG * MC > 1) {
+    if (cs > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = CG * MC;
+        attr[na].val.clusterDim.x = unsigned(cs);
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -66,18 +70,43 @@ cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &para
     ++na;
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT>, params);
+    void *args[1] = {const_cast<KernelParams *>(&params)};
+    return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
-#define GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, CT)                                                          \
-    Variant                                                                                                 \
-    {                                                                                                       \
-        CG, BN, ST, MC, (BK ? 0 : 1), (CT ? 1 : 0), KernelCfg<CG, BN, ST, MC, BK, CF, CT>::kSmemBytes,      \
-            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT>),                \
-            &launch_variant<CG, BN, ST, MC, BK, CF, CT>                                                     \
+template <int CG, int BN, int ST, int MC, bool BK, bool CF, bool CT, int EP>
+cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
+{
+    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP>),
+                             plan, params, stream, kNumThreads,
+                             KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes, CG * MC);
+}
+
+template <int ST>
+cudaError_t launch_wide(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
+{
+    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST>), plan, params, stream,
+                             kWideThreads, WideCfg<ST>::kSmemBytes, 2);
+}
+
+#define GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, EP)                                                        \
+    Variant                                                                                                   \
+    {                                                                                                         \
+        CG, BN, ST, MC, (BK ? 0 : 1), (CT ? 1 : 0), KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes,    \
+            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP>),              \
+            &launch_variant<CG, BN, ST, MC, BK, CF, CT, EP>, kNumThreads,                                     \
+            KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kBSlice                                                \
     }
+#define GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, CT) GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, 2)
 #define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF) GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, false)
 #define GEMM_VARIANT(CG, BN, ST, MC) GEMM_VARIANT_L(CG, BN, ST, MC, true, true)
+#define GEMM_VARIANT_WIDE(ST)                                                                                  \
+    Variant                                                                                                    \
+    {                                                                                                          \
+        2, WideCfg<ST>::kBN, ST, 1, 0, 0, WideCfg<ST>::kSmemBytes,                                             \
+            reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST>), &launch_wide<ST>, kWideThreads,      \
+            WideCfg<ST>::kBBoxRows                                                                             \
+    }
 
 const Variant kVariants[] = {
     GEMM_VARIANT(1, 256, 4, 1),  // 0: 128 x 256 tile, one CTA
@@ -98,6 +127,8 @@ const Variant kVariants[] = {
     // operands swapped (C^T = B . A^T, tiles stored transposed), for few rows of A
     GEMM_VARIANT_X(2, 128, 8, 1, true, true, true),  // 13: B rows on the pair's M = 256, A rows on N = 128
     GEMM_VARIANT_X(1, 128, 6, 1, true, true, true),  // 14: one CTA, 128 B rows x 128 A rows
+    // 256 x 512 tile on a CTA pair, one accumulator filling tensor memory (no stream-K tail)
+    GEMM_VARIANT_WIDE(4),  // 15
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -148,7 +179,7 @@ gemm_status_t device_info(DeviceInfo **out)
                     cudaLaunchConfig_t cfg;
                     memset(&cfg, 0, sizeof(cfg));
                     cfg.gridDim = dim3(unsigned(cs * (sms / cs)), 1, 1);
-                    cfg.blockDim = dim3(kNumThreads, 1, 1);
+                    cfg.blockDim = dim3(unsigned(var.threads), 1, 1);
                     cfg.dynamicSmemBytes = size_t(var.smem);
                     cudaLaunchAttribute attr;
                     attr.id = cudaLaunchAttributeClusterDimension;
@@ -345,8 +376,11 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.workspace_bytes = 0;
     p.k_rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks) ? 1 : 0;
     // the stream-K tail would not rotate: keep whole rotated tiles where rotation pays
+    // the wide variant has no stream-K tail: asking for one is an error, the automatic choice skips it
+    const bool sk_capable = var.bn <= 256;
+    if (stream_k == 1 && !sk_capable) return GEMM_ERR_INVALID_ARG;
     const bool want_sk = stream_k == 1 ||
-                         (stream_k < 0 && !p.k_rotate && streamk_pays(p.num_tiles, p.k_blocks, slots));
+                         (stream_k < 0 && sk_capable && !p.k_rotate && streamk_pays(p.num_tiles, p.k_blocks, slots));
     if (want_sk && p.num_tiles > 0) {
         // whole waves but the last one or two stay data-parallel; the rest is split evenly
         const int64_t full_waves = p.num_tiles / slots;
@@ -445,7 +479,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
             return GEMM_ERR_INVALID_ARG;
     } else {
         // owners wait for contributors: every cluster must be resident at once
-        if (plan.stream_k != 1 || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
+        if (plan.stream_k != 1 || kVariants[plan.variant].bn > 256 || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
             plan.sk_iters != (plan.num_tiles - plan.dp_tiles) * plan.k_blocks || plan.sk_iters < workers ||
             workers > dev->max_clusters[plan.variant] ||
             int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, kVariants[plan.variant].bn))
@@ -468,8 +502,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
                        uint32_t((var.cg == 1 && var.mc > 1) ? 128 / var.mc : 128));
     if (st != GEMM_OK) return st;
     if (var.layout == 0) {
-        st = encode_matrix(enc, &params.tmap_b, kb, uint64_t(kn), uint64_t(plan.k), kBlockK,
-                           uint32_t(var.bn / var.cg / (var.cg == 2 ? var.mc : 1)));
+        st = encode_matrix(enc, &params.tmap_b, kb, uint64_t(kn), uint64_t(plan.k), kBlockK, uint32_t(var.b_box));
         if (st != GEMM_OK) return st;
         if (var.swap)  // C [m, n] written in transposed tiles: boxes of 32 columns x 64 rows, unswizzled
             st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, 64, false);

@@ -108,7 +108,8 @@ struct KernelParams {
     uint32_t *error_word;
 };
 
-template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true, bool C_TRANS = false>
+template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true, bool C_TRANS = false,
+          int EPI = 2>
 struct KernelCfg {
     static_assert(CG == 1 || CG == 2, "cta group");
     static_assert(MC == 1 || MC == 2 || MC == 4, "cluster multicast width");
@@ -130,7 +131,10 @@ struct KernelCfg {
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
     static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, drain
-    static constexpr int kOffBar = kOffStore + kEpiWarps * 2 * kStoreBufBytes;
+    // EPI staging buffers per epilogue warp: 2 lets a warp fill one while the other is being stored;
+    // 1 frees 16 KB for one more ring stage
+    static_assert(EPI == 1 || EPI == 2, "epilogue staging buffers");
+    static constexpr int kOffBar = kOffStore + kEpiWarps * EPI * kStoreBufBytes;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
@@ -240,10 +244,10 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS>
+template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS>;
+    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>;
     constexpr int CS = Cfg::kCS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     } else {
         // ------------------------------------------------ epilogue
         const uint32_t quarter = warp & 3u;  // tensor-memory lanes [32q, 32q + 32) belong to this warp
-        const uint32_t stage_base = base + Cfg::kOffStore + (warp - 2u) * 2u * kStoreBufBytes;
+        const uint32_t stage_base = base + Cfg::kOffStore + (warp - 2u) * uint32_t(EPI) * kStoreBufBytes;
         const uint32_t lane_sel = (quarter * 32u) << 16;
         constexpr uint32_t kSlotFloats = 128u * BN;          // one CTA's partial tile
         constexpr uint32_t kChunkFloats = 32u * kStoreCols;  // one warp's 32 x 64 piece
@@ -528,8 +532,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                             // The tile is D' = C^T: lane = a column n of C, register j = row m of C.
                             // Stage a [64 m][32 n] fp16 block (64-byte rows, unswizzled), store it
                             // with a {32 n, 64 m} box at (n = row0, m = col).
-                            const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
-                            if (lane == 0) ptx::bulk_wait_group_read<1>();
+                            const uint32_t buf = stage_base + (EPI == 2 ? (stores & 1u) : 0u) * kStoreBufBytes;
+                            if (lane == 0) ptx::bulk_wait_group_read<EPI - 1>();
                             __syncwarp();
 #pragma unroll
                             for (int j = 0; j < W; ++j)
@@ -549,8 +553,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
 #pragma unroll
                             for (int h = 0; h < W / 32; ++h) {
                                 if (col + 32u * h >= p.n) break;
-                                const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
-                                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                                const uint32_t buf = stage_base + (EPI == 2 ? (stores & 1u) : 0u) * kStoreBufBytes;
+                                if (lane == 0) ptx::bulk_wait_group_read<EPI - 1>();
                                 __syncwarp();
                                 const uint32_t row_addr = buf + lane * 128u;
 #pragma unroll
@@ -568,8 +572,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                             }
                             return;
                         }
-                        const uint32_t buf = stage_base + (stores & 1u) * kStoreBufBytes;
-                        if (lane == 0) ptx::bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                        const uint32_t buf = stage_base + (EPI == 2 ? (stores & 1u) : 0u) * kStoreBufBytes;
+                        if (lane == 0) ptx::bulk_wait_group_read<EPI - 1>();  // this buffer's previous store has read it
                         __syncwarp();
                         if constexpr (W == 64) {
                             const uint32_t row_addr = buf + lane * 128u;
