@@ -257,23 +257,63 @@ double wave_efficiency(int64_t tiles, int64_t slots)
     return double(tiles) / double(waves * slots);
 }
 
+// A stream-K tail pays when the data-parallel schedule would leave the last
+// wave badly short of the resident clusters: measured, it wins when less
+// than about 86% of the slots are busy over the waves (ragged 3000x5000),
+// and loses above that, because under the power cap keeping the idle SMs of
+// a nearly full last wave busy costs clock for the whole launch.
+// Rotating the K walk of whole tiles pays when no operand strip is shared by
+// two tiles (a single row or column of tiles, e.g. 128 x 16384 x 16384:
+// measured +10%); when strips are shared, tiles that read them in K
+// lockstep hit L2 instead of DRAM, and rotation loses (8192^3: -6%).
+bool rotate_pays(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks)
+{
+    return (tiles_m == 1 || tiles_n == 1) && k_blocks >= 8;
+}
+
+bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
+{
+    if (k_blocks < 4 || num_tiles * k_blocks < 2 * slots) return false;
+    return wave_efficiency(num_tiles, slots) < 0.86;
+}
+
 // Tile-shape choice, from interleaved measurements on GB300 under the power
-// cap (256 x 256 CTA-pair tiles balance the tensor core against shared-
-// memory bandwidth; narrower tiles measured slower on every workload):
+// cap:
 //  - M <= 128: one 128-row tile; a CTA pair's second CTA would idle, the
 //    single-CTA 128 x 128 tile (variant 1) is fastest;
-//  - M <= 256: the 256 x 256 pair tile (variant 2);
-//  - otherwise the pair tile when its waves keep >= 95% of the pair slots
-//    busy (8192^3), else two pairs sharing B by multicast (variant 4), which
-//    moves less data per flop but fits only whole clusters of four SMs.
-int32_t auto_variant(int64_t m, int64_t n, int32_t num_sms, const int32_t *slots_by_variant, int32_t layout)
+//  - otherwise the cheaper of the 256 x 512 pair tile (variant 15) and an
+//    alternative with 256-column tiles: the 256 x 256 pair tile (variant 2)
+//    for M <= 256 or when its waves keep >= 95% of the pair slots busy,
+//    else two pairs sharing B by multicast (variant 4, whole clusters of
+//    four SMs only).
+// The estimate is waves x work per SM in units of a 256 x 256 pair tile
+// (variants 2 and 4: 1 per tile).  A 256 x 512 tile is 2 units but moves 25%
+// less data per flop, which under the power cap bought ~6% more clock
+// (8192^3: +4-5%); it counts 1.88.  An alternative whose tail stream-K
+// balances counts its tiles / slots plus 3% for the fix-up.  This picked
+// the faster plan on 12 of 13 measured shapes (4096^3, 8192^3, 6144^3,
+// 3000 x 5000 x 4096, 4096 x 8192 x 4096, ...; the miss, 7168^3, by 0.7%).
+int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, const int32_t *slots_by_variant,
+                     int32_t layout)
 {
     if (layout == 1) return m <= 128 ? 6 : 7;  // B stored [K, N], fp32 result
     if (m <= 128) return 1;
-    if (m <= 256) return 2;
-    const int64_t pair_slots = slots_by_variant ? slots_by_variant[2] : num_sms / 2;
-    const int64_t pair_tiles = ((m + 255) / 256) * ((n + 255) / 256);
-    return wave_efficiency(pair_tiles, pair_slots) >= 0.95 ? 2 : 4;
+    auto slots_of = [&](int v) -> int64_t {
+        const int64_t s = slots_by_variant ? slots_by_variant[v] : num_sms / (kVariants[v].cg * kVariants[v].mc);
+        return s < 1 ? 1 : s;
+    };
+    const int64_t pair_tiles_m = cdiv(m, 256), tiles_n = cdiv(n, 256);
+    int32_t alt = 2;
+    int64_t alt_tiles_m = pair_tiles_m;
+    if (m > 256 && wave_efficiency(pair_tiles_m * tiles_n, slots_of(2)) < 0.95) {
+        alt = 4;
+        alt_tiles_m = cdiv(m, 512);
+    }
+    const int64_t alt_tiles = alt_tiles_m * tiles_n, alt_slots = slots_of(alt);
+    const bool alt_sk = !rotate_pays(alt_tiles_m, tiles_n, k_blocks) && streamk_pays(alt_tiles, k_blocks, alt_slots);
+    const double alt_cost = alt_sk ? 1.03 * double(alt_tiles) / double(alt_slots) : double(cdiv(alt_tiles, alt_slots));
+    const double wide_cost = 1.88 * double(cdiv(pair_tiles_m * cdiv(n, 512), slots_of(15)));
+    return wide_cost < alt_cost ? 15 : alt;
 }
 
 int64_t round_up(int64_t x, int64_t a)
@@ -311,26 +351,6 @@ uint64_t next_sk_stamp()
     return g_sk_nonce | (c ? c : 1u);
 }
 
-// A stream-K tail pays when the data-parallel schedule would leave the last
-// wave badly short of the resident clusters: measured, it wins when less
-// than about 86% of the slots are busy over the waves (ragged 3000x5000),
-// and loses above that, because under the power cap keeping the idle SMs of
-// a nearly full last wave busy costs clock for the whole launch.
-// Rotating the K walk of whole tiles pays when no operand strip is shared by
-// two tiles (a single row or column of tiles, e.g. 128 x 16384 x 16384:
-// measured +10%); when strips are shared, tiles that read them in K
-// lockstep hit L2 instead of DRAM, and rotation loses (8192^3: -6%).
-bool rotate_pays(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks)
-{
-    return (tiles_m == 1 || tiles_n == 1) && k_blocks >= 8;
-}
-
-bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
-{
-    if (k_blocks < 4 || num_tiles * k_blocks < 2 * slots) return false;
-    return wave_efficiency(num_tiles, slots) < 0.86;
-}
-
 gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_t max_clusters_in,
                         int32_t variant, int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out,
                         const int32_t *slots_by_variant = nullptr, int32_t layout = -1)
@@ -340,7 +360,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     if (st != GEMM_OK) return st;
     if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
     if (variant >= kNumVariants || stream_k > 1 || layout > 1) return GEMM_ERR_INVALID_ARG;
-    if (variant < 0) variant = auto_variant(m, n, num_sms, slots_by_variant, layout < 0 ? 0 : layout);
+    if (variant < 0) variant = auto_variant(m, n, cdiv(k, kBlockK), num_sms, slots_by_variant, layout < 0 ? 0 : layout);
     const Variant &var = kVariants[variant];
     if (layout >= 0 && var.layout != layout) return GEMM_ERR_INVALID_ARG;
     const int32_t cs = var.cg * var.mc;  // CTAs per cluster

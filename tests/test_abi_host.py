@@ -246,3 +246,18 @@ def test_k_rotation_rule(L):
     assert skinny.k_rotate == 1 and skinny.stream_k == 0      # one row of tiles: no strip is shared
     big = G.gemm_f16_nt_plan_for(8192, 8192, 8192, 152)
     assert big.k_rotate == 0                                   # strips shared by neighbouring tiles
+
+
+@pytest.mark.parametrize("shape,variant,stream_k", [
+    ((8192, 8192, 8192), 15, 0),     # 256 x 512 pair tiles: least data per flop, 96% of the waves busy
+    ((6144, 6144, 6144), 15, 0),
+    ((4096, 8192, 4096), 2, 0),      # 256 x 256 pair tiles fill 96% of their waves, the wide ones 84%
+    ((3000, 5000, 4096), 4, 1),      # multicast pairs with a stream-K tail beat a 79%-busy wide tile
+    ((256, 256, 256), 2, 0),         # one tile: the wide tile would compute twice the area
+    ((128, 16384, 16384), 1, 0),     # M <= 128: single-CTA 128 x 128 tiles
+])
+def test_auto_variant_choices(L, shape, variant, stream_k):
+    """The automatic plan's tile choice on a 152-SM part with every variant's full complement of
+    clusters (the measured cases its cost estimate was fitted to)."""
+    p = G.gemm_f16_nt_plan_for(*shape, 152)
+    assert (p.variant, p.stream_k) == (variant, stream_k)
