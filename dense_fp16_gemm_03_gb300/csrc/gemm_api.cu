@@ -639,6 +639,85 @@ gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int3
     return make_plan(m, n, k, dev->num_sms, 0, variant, raster_width, stream_k, out, dev->max_clusters, layout);
 }
 
+// ---------------------------------------------- host-buffer pipeline
+
+// gemm_f16_nt_host moves the rows of A and C through in chunks so that the
+// copies of one chunk overlap the GEMM of another: B and the first rows of A
+// go in first; then chunk i's GEMM runs on the caller's stream while chunk
+// i+1's rows of A come in on one copy stream and chunk i-1's rows of C go out
+// on another.  On GB300 the copy engines move ~210 GB/s in and ~190 GB/s out
+// (~170 each way at once) and run beside the GEMM at full speed, so the step
+// time falls from copies + GEMM towards the inbound copy time.
+constexpr int kHostChunksMax = 8;
+constexpr int64_t kHostChunkRowsMin = 1024;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;  // inbound and outbound copy streams
+    cudaEvent_t start = nullptr, in_done = nullptr, out_done = nullptr;
+    cudaEvent_t landed[kHostChunksMax] = {};    // chunk i's rows of A (and all of B) are on the device
+    cudaEvent_t computed[kHostChunksMax] = {};  // chunk i's rows of C are computed
+};
+
+std::mutex g_pipe_mutex;
+HostPipe g_pipes[kMaxDevices];
+
+// The current device's copy streams and events, created on first use; call
+// with g_pipe_mutex held.
+gemm_status_t host_pipe(HostPipe **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    HostPipe &hp = g_pipes[dev];
+    if (!hp.ready) {
+        HostPipe made;
+        bool ok = cudaStreamCreateWithFlags(&made.in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&made.out, cudaStreamNonBlocking) == cudaSuccess;
+        cudaEvent_t *events[3 + 2 * kHostChunksMax] = {&made.start, &made.in_done, &made.out_done};
+        for (int i = 0; i < kHostChunksMax; ++i) {
+            events[3 + 2 * i] = &made.landed[i];
+            events[4 + 2 * i] = &made.computed[i];
+        }
+        for (cudaEvent_t *e : events)
+            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            for (cudaEvent_t *e : events)
+                if (*e) cudaEventDestroy(*e);
+            if (made.in) cudaStreamDestroy(made.in);
+            if (made.out) cudaStreamDestroy(made.out);
+            return GEMM_ERR_CUDA;
+        }
+        made.ready = true;
+        hp = made;
+    }
+    *out = &hp;
+    return GEMM_OK;
+}
+
+// Rows per chunk: whole 256-row tiles, at least 1024 rows, at most 8 chunks.
+int64_t host_chunk_rows(int64_t m)
+{
+    int64_t chunks = m / kHostChunkRowsMin;
+    if (chunks < 1) chunks = 1;
+    if (chunks > kHostChunksMax) chunks = kHostChunksMax;
+    return round_up(cdiv(m, chunks), 256);
+}
+
+// The automatic plan for a chunk, without a stream-K tail when the caller's
+// workspace cannot hold one.
+gemm_status_t chunk_plan(int64_t m, int64_t n, int64_t k, const void *workspace, size_t ws_bytes,
+                         gemm_f16_plan_t *p)
+{
+    gemm_status_t st = device_plan(m, n, k, -1, 0, -1, p);
+    if (st == GEMM_OK && p->workspace_bytes > 0 && (!workspace || ws_bytes < p->workspace_bytes))
+        st = device_plan(m, n, k, -1, 0, 0, p);
+    return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -752,19 +831,80 @@ gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_ho
     if (m == 0 || n == 0) return GEMM_OK;
     if (!c_host || (k > 0 && (!a_host || !b_host))) return GEMM_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (k > 0) {
-        if (cudaMemcpyAsync(a_dev, a_host, size_t(m) * size_t(k) * 2u, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpyAsync(b_dev, b_host, size_t(n) * size_t(k) * 2u, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    const int64_t rows = host_chunk_rows(m);
+    const int64_t chunks = cdiv(m, rows);
+    if (k == 0 || chunks == 1) {
+        // one chunk: copies in, GEMM, copy out, in stream order
+        if (k > 0) {
+            if (cudaMemcpyAsync(a_dev, a_host, size_t(m) * size_t(k) * 2u, cudaMemcpyHostToDevice, s) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(b_dev, b_host, size_t(n) * size_t(k) * 2u, cudaMemcpyHostToDevice, s) !=
+                    cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+        }
+        st = workspace ? gemm_f16_nt_ws(m, n, k, a_dev, b_dev, c_dev, workspace, ws_bytes, stream)
+                       : gemm_f16_nt(m, n, k, a_dev, b_dev, c_dev, stream);
+        if (st != GEMM_OK) return st;
+        if (cudaMemcpyAsync(c_host, c_dev, size_t(m) * size_t(n) * 2u, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
+        return GEMM_OK;
     }
-    st = workspace ? gemm_f16_nt_ws(m, n, k, a_dev, b_dev, c_dev, workspace, ws_bytes, stream)
-                   : gemm_f16_nt(m, n, k, a_dev, b_dev, c_dev, stream);
+    // the plans first, so that a planning error enqueues nothing
+    gemm_f16_plan_t plan_full, plan_last;
+    const int64_t last_rows = m - (chunks - 1) * rows;
+    st = chunk_plan(rows, n, k, workspace, ws_bytes, &plan_full);
+    if (st == GEMM_OK) st = chunk_plan(last_rows, n, k, workspace, ws_bytes, &plan_last);
     if (st != GEMM_OK) return st;
-    if (cudaMemcpyAsync(c_host, c_dev, size_t(m) * size_t(n) * 2u, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe *hp = nullptr;
+    st = host_pipe(&hp);
+    if (st != GEMM_OK) return st;
+    const char *ah = static_cast<const char *>(a_host);
+    char *ad = static_cast<char *>(a_dev), *ch = static_cast<char *>(c_host), *cd = static_cast<char *>(c_dev);
+    const size_t a_row = size_t(k) * 2u, c_row = size_t(n) * 2u;
+    bool ok = true;
+    auto cuda_ok = [&](cudaError_t e) {
+        if (e != cudaSuccess) ok = false;
+        return ok;
+    };
+    // both copy streams start after the work the caller has already enqueued on `stream`
+    cuda_ok(cudaEventRecord(hp->start, s)) && cuda_ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) &&
+        cuda_ok(cudaStreamWaitEvent(hp->out, hp->start, 0)) &&
+        cuda_ok(cudaMemcpyAsync(b_dev, b_host, size_t(n) * size_t(k) * 2u, cudaMemcpyHostToDevice, hp->in));
+    for (int64_t i = 0; ok && i < chunks; ++i) {
+        const int64_t r = (i + 1 < chunks) ? rows : last_rows;
+        cuda_ok(cudaMemcpyAsync(ad + size_t(i * rows) * a_row, ah + size_t(i * rows) * a_row, size_t(r) * a_row,
+                                cudaMemcpyHostToDevice, hp->in)) &&
+            cuda_ok(cudaEventRecord(hp->landed[i], hp->in));
+    }
+    for (int64_t i = 0; ok && i < chunks; ++i) {
+        const bool last = (i + 1 == chunks);
+        const gemm_f16_plan_t &p = last ? plan_last : plan_full;
+        const int64_t r = last ? last_rows : rows;
+        if (!cuda_ok(cudaStreamWaitEvent(s, hp->landed[i], 0))) break;
+        st = run_plan(p, ad + size_t(i * rows) * a_row, b_dev, cd + size_t(i * rows) * c_row, workspace, ws_bytes, s,
+                      ~0u, default_wait_limit(p.k_blocks));
+        if (st != GEMM_OK) {
+            ok = false;
+            break;
+        }
+        cuda_ok(cudaEventRecord(hp->computed[i], s)) && cuda_ok(cudaStreamWaitEvent(hp->out, hp->computed[i], 0)) &&
+            cuda_ok(cudaMemcpyAsync(ch + size_t(i * rows) * c_row, cd + size_t(i * rows) * c_row, size_t(r) * c_row,
+                                    cudaMemcpyDeviceToHost, hp->out));
+    }
+    // the caller's stream continues after the last copy in and the last copy out (joined even
+    // after an error, so that nothing enqueued here outlives the call's place in the stream)
+    const bool joined = cudaEventRecord(hp->in_done, hp->in) == cudaSuccess &&
+                        cudaEventRecord(hp->out_done, hp->out) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, hp->in_done, 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, hp->out_done, 0) == cudaSuccess;
+    if (!ok || !joined) {
         cudaGetLastError();
-        return GEMM_ERR_CUDA;
+        return st != GEMM_OK ? st : GEMM_ERR_CUDA;
     }
     return GEMM_OK;
 }

@@ -185,10 +185,19 @@ gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const 
 /*
  * End-to-end form for host-resident data: copies a_host (M*K fp16) and
  * b_host (N*K fp16) into the caller's device buffers a_dev / b_dev, runs
- * the GEMM into c_dev (as gemm_f16_nt_ws with the given workspace, which
- * may be NULL/0), and copies c_dev back to c_host (M*N fp16), all enqueued
- * on `stream` (asynchronous; pinned host memory makes the copies truly
- * asynchronous).  Allocates nothing.
+ * the GEMM into c_dev (automatic plan; the workspace, which may be NULL/0,
+ * serves a stream-K tail when it is large enough), and copies c_dev back to
+ * c_host (M*N fp16).  Asynchronous on `stream`: the work starts after what
+ * is already enqueued there and the stream continues after the last copy
+ * back; pinned host memory makes the copies truly asynchronous.
+ *
+ * From M >= 2048 the rows of A and C go through in 2 to 8 chunks of whole
+ * 256-row tiles, so that the copies overlap the GEMMs: B and the first rows
+ * of A are copied in first, then chunk i's GEMM runs on `stream` while the
+ * rows of chunk i+1 come in on an internal copy stream and those of chunk
+ * i-1 go out on another.  The two copy streams and their events are created
+ * on the first such call for each device and kept; buffers are never
+ * allocated.  Calls from several host threads are enqueued one at a time.
  */
 gemm_status_t gemm_f16_nt_host(int64_t m, int64_t n, int64_t k, const void *a_host,
                                const void *b_host, void *c_host, void *a_dev, void *b_dev,

@@ -240,6 +240,39 @@ def test_side_stream_and_host_entry_point():
     assert_parity(c_h.view(torch.int16).numpy().view(np.uint16), A, B, exact=True)
 
 
+@pytest.mark.parametrize("shape", [(2048, 1032, 520), (3000, 520, 264), (4096, 1024, 512), (8192, 264, 136)])
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_host_entry_point_chunked(shape, use_ws):
+    """From 2048 rows on, the host-buffer entry point moves A and C through in row chunks on two
+    copy streams beside the GEMMs (ragged last chunk included); back-to-back calls with different
+    operands on one stream must not overwrite device buffers a previous call still reads, and the
+    caller's stream must continue only after the last copy out."""
+    M, N, K = shape
+    s = torch.cuda.Stream()
+    a_d = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    b_d = torch.empty((N, K), dtype=torch.float16, device="cuda")
+    c_d = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = None
+    if use_ws:
+        ws = torch.empty(max(256, G.gemm_f16_nt_workspace_size(M, N, K)), dtype=torch.uint8, device="cuda")
+    pairs, outs = [], []
+    for seed in (31, 32, 33):
+        A, B = inputs.make_operands(M, N, K, "eighths", seed=seed + M)
+        a_h = torch.from_numpy(A.view(np.int16)).view(torch.float16).pin_memory()
+        b_h = torch.from_numpy(B.view(np.int16)).view(torch.float16).pin_memory()
+        c_h = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+        pairs.append((A, B, a_h, b_h))                                   # host buffers live until the sync
+        outs.append(c_h)
+        G.gemm_f16_nt_host(a_h, b_h, c_h, a_d, b_d, c_d, ws, stream=s)     # no sync between calls
+    with torch.cuda.stream(s):
+        c_dev_copy = c_d.clone()                                          # ordered after the last call
+    s.synchronize()
+    assert G.gemm_f16_take_device_error()[0] == G.GEMM_OK
+    for (A, B, _, _), c_h in zip(pairs, outs):
+        assert_parity(c_h.view(torch.int16).numpy().view(np.uint16), A, B, exact=True)
+    assert torch.equal(c_dev_copy.cpu().view(torch.int16), outs[-1].view(torch.int16))
+
+
 def test_plan_matches_device():
     p = G.gemm_f16_nt_plan(8192, 8192, 8192)
     assert p.num_sms == num_sms()
