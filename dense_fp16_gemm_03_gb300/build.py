@@ -3,6 +3,7 @@
 One translation unit, one ``-gencode`` (sm_103a), shared cudart; nvcc
 cross-compiles it on a machine without a GPU.
 """
+import glob
 import os
 import subprocess
 import sys
@@ -14,9 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm_f16.so")
 SOURCES = [os.path.join(CSRC, "gemm_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_kernel.cuh", "ptx.cuh", "sched.cuh")] + [
-    os.path.join(INCLUDE, "gemm_f16.h")
-]
+DEPS = SOURCES + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "gemm_f16.h")]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = [
