@@ -236,7 +236,7 @@ ABLATION = [
     ("CTA pair, six stages", "-", 2, 1, True),
     ("persistent: epilogue overlaps the next tile, raster 8", "-", 2, 8, False),
     ("persistent, two pairs share B by multicast", "-", 4, 8, False),
-    ("persistent 256 x 512 pair tile, one accumulator filling tensor memory", "-", 15, 8, False),
+    ("persistent 256 x 512 pair tile, one accumulator filling tensor memory, raster 4", "-", 15, 4, False),
 ]
 
 

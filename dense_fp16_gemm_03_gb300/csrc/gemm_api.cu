@@ -238,13 +238,15 @@ int64_t cdiv(int64_t a, int64_t b)
 
 // --------------------------------------------------------------- plans
 
-// Raster width: N-columns per raster group.  Measured on GB300 (8192^3,
-// 256 x 256 pair tiles, interleaved runs under the power cap): widths 8-16
-// kept the clock highest (fewest DRAM re-reads) and gave the best
-// throughput; 1-4 re-read A from DRAM more often.
-int32_t auto_raster_width(int64_t tiles_n)
+// Raster width: tile columns per raster group, so that a group spans 2048
+// columns of C.  Measured on GB300 (interleaved runs under the power cap):
+// 256-column pair tiles at 8192^3 did best with widths 8-16 (fewest DRAM
+// re-reads, highest clock), 512-column tiles with width 4 (8192^3: +1% over
+// width 8; 4096^3 and 6144^3 level or slightly ahead); narrower groups re-read
+// A from DRAM more often.
+int32_t auto_raster_width(int64_t tiles_n, int32_t block_n)
 {
-    int64_t w = 8;
+    int64_t w = 2048 / (block_n > 0 ? block_n : 256);
     if (w > tiles_n) w = tiles_n;
     return int32_t(w < 1 ? 1 : w);
 }
@@ -415,7 +417,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
         }
     }
     p.grid = int32_t(clusters * cs);
-    if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_n);
+    if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_n, p.block_n);
     if (p.tiles_n > 0 && raster_width > p.tiles_n) raster_width = int32_t(p.tiles_n);
     if (raster_width < 1) raster_width = 1;
     p.raster_width = raster_width;

@@ -246,10 +246,12 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                     }
                 }
             }
-            // tensor memory is free for the next tile as soon as every warp has read its piece
+            // tensor memory is free for the next tile as soon as every warp has read its piece; the
+            // loads are complete (tcgen05.wait::ld), so the arrival only signals, with CTA-scope
+            // release: a cluster-scope one stalled each warp ~950 cycles while the MMA warp waited
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_rank(bar_acc_empty, 0u));
+            if (lane == 0) ptx::mbar_arrive_cluster_signal(ptx::map_to_rank(bar_acc_empty, 0u));
             if (live) {
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
