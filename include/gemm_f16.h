@@ -74,8 +74,10 @@ typedef enum gemm_status {
 typedef struct gemm_f16_plan {
     int32_t variant;         /* compiled kernel instance, see gemm_f16_variant_info */
     int32_t cta_group;       /* 1: one CTA per MMA tile; 2: a CTA pair (cluster of 2) shares one */
-    int32_t block_m;         /* output rows per MMA tile (128 * cta_group) */
-    int32_t block_n;         /* output columns per MMA tile */
+    int32_t block_m;         /* output rows per cluster tile (128 * cta_group, times the CTA pairs a
+                                multicast cluster stacks along M) */
+    int32_t block_n;         /* output columns per cluster tile (the 256 x 512 tile: 512, two MMAs of N = 256;
+                                single CTAs sharing A by multicast: N times the CTAs along N) */
     int32_t block_k;         /* K depth of one pipeline stage (64) */
     int32_t stages;          /* shared-memory ring depth */
     int32_t raster_width;    /* N-columns per raster group (>= 1) */
@@ -89,7 +91,7 @@ typedef struct gemm_f16_plan {
     int64_t dp_tiles;        /* tiles walked data-parallel (all of them when stream_k == 0) */
     int64_t sk_iters;        /* K-block iterations of the remaining tiles, split evenly over the clusters */
     int32_t grid;            /* CTAs launched (persistent: <= resident slots) */
-    int32_t cluster;         /* CTAs per cluster (= cta_group) */
+    int32_t cluster;         /* CTAs per cluster (cta_group times the multicast width) */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t num_sms;         /* SM count the plan was made for */
     uint64_t workspace_bytes;/* device workspace the plan needs (0 = none) */
@@ -109,7 +111,9 @@ typedef struct gemm_f16_plan {
  * shared by launches that overlap on the GPU.  Every cluster of the grid
  * must be resident at once; the plan's
  * grid never exceeds that.  The fp32 partial sums change the rounding order
- * of split tiles only within the fp32 accumulation error.
+ * of split tiles only within the fp32 accumulation error.  The 256 x 512
+ * tile (block_n 512) has no stream-K tail: asking for one is
+ * GEMM_ERR_INVALID_ARG, and automatic plans never give it one.
  */
 
 /* Human-readable name of a status code (static string, never NULL). */
