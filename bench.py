@@ -37,9 +37,9 @@ UNIT = "TFLOP/s"
 NOMINAL_PEAK_TFLOPS = 2250.0      # dense fp16/bf16 tensor peak quoted for GB300
 FALLBACK_PEAK_TFLOPS = 1700.0     # bf16 sustained, measured earlier on a GB300
 L2_BYTES = 129 * 10 ** 6
-KERNEL_SOURCES = ["dense_fp16_gemm_03_gb300/csrc/gemm_kernel.cuh", "dense_fp16_gemm_03_gb300/csrc/ptx.cuh",
-                  "dense_fp16_gemm_03_gb300/csrc/sched.cuh", "dense_fp16_gemm_03_gb300/csrc/gemm_api.cu",
-                  "dense_fp16_gemm_03_gb300/csrc/gemm_kernel_wide.cuh"]
+KERNEL_SOURCES = ["dense_fp16_gemm_03_gb300/csrc/gemm_kernel.cuh", "dense_fp16_gemm_03_gb300/csrc/gemm_kernel_wide.cuh",
+                  "dense_fp16_gemm_03_gb300/csrc/ptx.cuh", "dense_fp16_gemm_03_gb300/csrc/sched.cuh",
+                  "dense_fp16_gemm_03_gb300/csrc/gemm_launch.cuh"]
 
 
 def kernel_source_hash():

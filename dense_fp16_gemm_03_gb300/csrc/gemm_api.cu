@@ -1,6 +1,8 @@
 // C ABI of the fp16 NT GEMM (declared in include/gemm_f16.h): argument
-// validation, planning (variant, raster width, grid), TMA tensor-map
-// encoding, and the launch of the persistent sm_103a kernel.
+// validation, planning (variant, raster width, grid, stream-K tail or
+// rotated K walk), the host-buffer pipeline and the allocation-free form;
+// the variant table, the launch and the TMA tensor maps are in
+// gemm_launch.cuh.
 //
 // The interface mirrors the call of "1. WGMMA: Hopper's Asynchronous Tensor
 // Core" (section "The Full Kernel": m, n, k and the a, b, c fp16 pointers)
@@ -18,8 +20,7 @@
 #include <string.h>
 
 #include "gemm_f16.h"
-#include "gemm_kernel.cuh"
-#include "gemm_kernel_wide.cuh"
+#include "gemm_launch.cuh"
 
 using namespace gemm_f16;
 
@@ -30,107 +31,6 @@ __device__ uint32_t g_gemm_f16_error_word = 0u;
 namespace {
 
 constexpr int kMaxDevices = 64;
-
-// ------------------------------------------------------------ variants
-
-struct Variant {
-    int cg, bn, stages, mc;
-    int layout;  // 0: B [N,K], fp16 C; 1: B [K,N], fp32 D
-    int swap;    // 1: computes C^T = B . A^T (operands swapped, tiles stored transposed)
-    int smem;
-    const void *fn;
-    cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
-    int threads;  // threads per CTA
-    int b_box;    // B rows per TMA box (B [N,K] layout)
-};
-
-// Launch `kernel` persistently with clusters of `cs` CTAs, as a programmatic dependent launch.
-cudaError_t launch_persistent(const void *kernel, const gemm_f16_plan_t &plan, const KernelParams &params,
-                              cudaStream_t stream, int threads, int smem, int cs)
-{
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(unsigned(plan.grid), 1, 1);
-    cfg.blockDim = dim3(unsigned(threads), 1, 1);
-    cfg.dynamicSmemBytes = size_t(smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (cs > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = unsigned(cs);
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    // programmatic dependent launch: the kernel's set-up may overlap the previous kernel's tail;
-    // it waits (griddepcontrol.wait) for that kernel before touching global memory
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    void *args[1] = {const_cast<KernelParams *>(&params)};
-    return cudaLaunchKernelExC(&cfg, kernel, args);
-}
-
-template <int CG, int BN, int ST, int MC, bool BK, bool CF, bool CT, int EP>
-cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
-{
-    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP>),
-                             plan, params, stream, kNumThreads,
-                             KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes, CG * MC);
-}
-
-template <int ST>
-cudaError_t launch_wide(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
-{
-    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST>), plan, params, stream,
-                             kWideThreads, WideCfg<ST>::kSmemBytes, 2);
-}
-
-#define GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, EP)                                                        \
-    Variant                                                                                                   \
-    {                                                                                                         \
-        CG, BN, ST, MC, (BK ? 0 : 1), (CT ? 1 : 0), KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes,    \
-            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP>),              \
-            &launch_variant<CG, BN, ST, MC, BK, CF, CT, EP>, kNumThreads,                                     \
-            KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kBSlice                                                \
-    }
-#define GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, CT) GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, 2)
-#define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF) GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, false)
-#define GEMM_VARIANT(CG, BN, ST, MC) GEMM_VARIANT_L(CG, BN, ST, MC, true, true)
-#define GEMM_VARIANT_WIDE(ST)                                                                                  \
-    Variant                                                                                                    \
-    {                                                                                                          \
-        2, WideCfg<ST>::kBN, ST, 1, 0, 0, WideCfg<ST>::kSmemBytes,                                             \
-            reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST>), &launch_wide<ST>, kWideThreads,      \
-            WideCfg<ST>::kBBoxRows                                                                             \
-    }
-
-const Variant kVariants[] = {
-    GEMM_VARIANT(1, 256, 4, 1),  // 0: 128 x 256 tile, one CTA
-    GEMM_VARIANT(1, 128, 6, 1),  // 1: 128 x 128 tile, one CTA
-    GEMM_VARIANT(2, 256, 6, 1),  // 2: 256 x 256 tile on a CTA pair
-    GEMM_VARIANT(2, 128, 8, 1),  // 3: 256 x 128 tile on a CTA pair
-    GEMM_VARIANT(2, 256, 6, 2),  // 4: two pairs stacked along M share B by multicast (512 x 256 per cluster)
-    GEMM_VARIANT(2, 224, 6, 2),  // 5: as 4 with 224-column tiles (512 x 224 per cluster)
-    // B stored [K, N] (MN-major operand), fp32 result
-    GEMM_VARIANT_L(1, 128, 6, 1, false, false),  // 6: 128 x 128 tile, one CTA
-    GEMM_VARIANT_L(2, 256, 6, 1, false, false),  // 7: 256 x 256 tile on a CTA pair
-    // shallow rings, for the pipeline-depth ablation only
-    GEMM_VARIANT(1, 128, 1, 1),  // 8: single stage: load, then compute, then load
-    GEMM_VARIANT(1, 128, 2, 1),  // 9: two stages
-    GEMM_VARIANT(2, 256, 3, 1),  // 10: CTA pair, three stages
-    GEMM_VARIANT(1, 128, 6, 2),  // 11: two CTAs along N share A by multicast (128 x 256 per cluster)
-    GEMM_VARIANT(1, 128, 6, 4),  // 12: four CTAs along N share A by multicast (128 x 512 per cluster)
-    // operands swapped (C^T = B . A^T, tiles stored transposed), for few rows of A
-    GEMM_VARIANT_X(2, 128, 8, 1, true, true, true),  // 13: B rows on the pair's M = 256, A rows on N = 128
-    GEMM_VARIANT_X(1, 128, 6, 1, true, true, true),  // 14: one CTA, 128 B rows x 128 A rows
-    // 256 x 512 tile on a CTA pair, one accumulator filling tensor memory (no stream-K tail)
-    GEMM_VARIANT_WIDE(4),  // 15
-};
-constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
 // ---------------------------------------------------- per-device state
 
@@ -279,6 +179,19 @@ bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
     return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
+// Rotation and a stream-K tail exclude each other (the tail does not rotate).
+// Rotation wins where it was measured to (one row or column of tiles filling
+// most of the machine, e.g. 128 x 16384 x 16384); when fewer than half of
+// the slots would have a tile (e.g. one 256 x 256 tile with K = 2^20), only
+// splitting K over the clusters keeps the machine busy, so the tail wins.
+void tail_choice(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks, int64_t slots, bool *rotate, bool *stream_k)
+{
+    const int64_t tiles = tiles_m * tiles_n;
+    const bool sk = streamk_pays(tiles, k_blocks, slots);
+    *rotate = rotate_pays(tiles_m, tiles_n, k_blocks) && !(sk && wave_efficiency(tiles, slots) < 0.5);
+    *stream_k = sk && !*rotate;
+}
+
 // Tile-shape choice, from interleaved measurements on GB300 under the power
 // cap:
 //  - M <= 128: one 128-row tile; a CTA pair's second CTA would idle, the
@@ -312,7 +225,8 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
         alt_tiles_m = cdiv(m, 512);
     }
     const int64_t alt_tiles = alt_tiles_m * tiles_n, alt_slots = slots_of(alt);
-    const bool alt_sk = !rotate_pays(alt_tiles_m, tiles_n, k_blocks) && streamk_pays(alt_tiles, k_blocks, alt_slots);
+    bool alt_rotate = false, alt_sk = false;
+    tail_choice(alt_tiles_m, tiles_n, k_blocks, alt_slots, &alt_rotate, &alt_sk);
     const double alt_cost = alt_sk ? 1.03 * double(alt_tiles) / double(alt_slots) : double(cdiv(alt_tiles, alt_slots));
     const double wide_cost = 1.88 * double(cdiv(pair_tiles_m * cdiv(n, 512), slots_of(15)));
     return wide_cost < alt_cost ? 15 : alt;
@@ -396,13 +310,16 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.dp_tiles = p.num_tiles;
     p.sk_iters = 0;
     p.workspace_bytes = 0;
-    p.k_rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks) ? 1 : 0;
-    // the stream-K tail would not rotate: keep whole rotated tiles where rotation pays
     // the wide variant has no stream-K tail: asking for one is an error, the automatic choice skips it
     const bool sk_capable = var.bn <= 256;
     if (stream_k == 1 && !sk_capable) return GEMM_ERR_INVALID_ARG;
-    const bool want_sk = stream_k == 1 ||
-                         (stream_k < 0 && sk_capable && !p.k_rotate && streamk_pays(p.num_tiles, p.k_blocks, slots));
+    // rotation or a stream-K tail (tail_choice); with the tail forbidden or unavailable, rotation alone
+    bool rotate = false, tail = false;
+    tail_choice(p.tiles_m, p.tiles_n, p.k_blocks, slots, &rotate, &tail);
+    if (stream_k == 0 || !sk_capable) rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks);
+    if (stream_k == 1) rotate = false;
+    p.k_rotate = rotate ? 1 : 0;
+    const bool want_sk = stream_k == 1 || (stream_k < 0 && sk_capable && tail);
     if (want_sk && p.num_tiles > 0) {
         // whole waves but the last one or two stay data-parallel; the rest is split evenly
         const int64_t full_waves = p.num_tiles / slots;
@@ -423,45 +340,6 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.raster_width = raster_width;
     *out = p;
     return GEMM_OK;
-}
-
-// ------------------------------------------------------- tensor maps
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-gemm_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
-{
-    static std::once_flag once;
-    std::call_once(once, []() {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-        else
-            cudaGetLastError();
-    });
-    *fn = g_encode;
-    return g_encode ? GEMM_OK : GEMM_ERR_CUDA;
-}
-
-// Row-major fp16 (or, with elem_bytes 4, fp32) matrix of `rows` x `cols`
-// (cols contiguous), boxes of box_cols x box_rows (128-byte swizzled unless
-// `swizzle` is false), zero fill outside the matrix.
-gemm_status_t encode_matrix(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *ptr,
-                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows, bool swizzle = true,
-                            uint32_t elem_bytes = 2)
-{
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * elem_bytes};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
 }
 
 gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b, void *c, void *ws,
@@ -510,37 +388,13 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     }
     const Variant &var = kVariants[plan.variant];
 
-    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    st = get_encoder(&enc);
-    if (st != GEMM_OK) return st;
     KernelParams params;
     memset(&params, 0, sizeof(params));
+    st = encode_tensor_maps(var, plan, a, b, c, &params);
+    if (st != GEMM_OK) return st;
     // kernel-side problem: the transposed one for a swapped variant
-    const void *ka = var.swap ? b : a;
-    const void *kb = var.swap ? a : b;
     const int64_t km = var.swap ? plan.n : plan.m;
     const int64_t kn = var.swap ? plan.m : plan.n;
-    st = encode_matrix(enc, &params.tmap_a, ka, uint64_t(km), uint64_t(plan.k), kBlockK,
-                       uint32_t((var.cg == 1 && var.mc > 1) ? 128 / var.mc : 128));
-    if (st != GEMM_OK) return st;
-    if (var.layout == 0) {
-        st = encode_matrix(enc, &params.tmap_b, kb, uint64_t(kn), uint64_t(plan.k), kBlockK, uint32_t(var.b_box));
-        if (st != GEMM_OK) return st;
-        if (var.swap)  // C [m, n] written in transposed tiles: boxes of 32 columns x 64 rows, unswizzled
-            st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, 64, false);
-        else
-            st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
-    } else {
-        // B [K, N]: 64-column boxes of 64 K rows; D [M, N] fp32: 32-column boxes
-        st = encode_matrix(enc, &params.tmap_b, b, uint64_t(plan.k), uint64_t(plan.n), 64, kBlockK);
-        if (st != GEMM_OK) return st;
-        st = encode_matrix(enc, &params.tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, true, 4);
-    }
-    if (st != GEMM_OK) return st;
-    if (var.bn % 64 != 0 && var.layout == 0) {
-        st = encode_matrix(enc, &params.tmap_c32, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, false);
-        if (st != GEMM_OK) return st;
-    }
     params.raster = make_raster(uint32_t(plan.tiles_m), uint32_t(plan.tiles_n), uint32_t(plan.raster_width));
     params.m = uint32_t(km);
     params.n = uint32_t(kn);

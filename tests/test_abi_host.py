@@ -254,7 +254,8 @@ def test_k_rotation_rule(L):
     ((4096, 8192, 4096), 2, 0),      # 256 x 256 pair tiles fill 96% of their waves, the wide ones 84%
     ((3000, 5000, 4096), 4, 1),      # multicast pairs with a stream-K tail beat a 79%-busy wide tile
     ((256, 256, 256), 2, 0),         # one tile: the wide tile would compute twice the area
-    ((128, 16384, 16384), 1, 0),     # M <= 128: single-CTA 128 x 128 tiles
+    ((128, 16384, 16384), 1, 0),     # M <= 128: single-CTA 128 x 128 tiles, rotated K walk
+    ((256, 256, 1 << 20), 2, 1),     # one tile: its K is split over every cluster instead of rotated
 ])
 def test_auto_variant_choices(L, shape, variant, stream_k):
     """The automatic plan's tile choice on a 152-SM part with every variant's full complement of
