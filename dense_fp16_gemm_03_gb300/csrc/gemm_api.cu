@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <chrono>
 #include <mutex>
 #include <random>
@@ -179,6 +180,22 @@ bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
     return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
+// Clusters that share a stream-K tail of `tiles` tiles when no whole wave is
+// left to run data-parallel.  A tile split over w clusters is finished by its
+// owner adding the other w - 1 partials one after another (~2,800 cycles each
+// for a CTA's 128 KB at 256 columns), while the split shortens every
+// cluster's K range (512 cycles per K block); both scale with the tile width.
+// Balancing tiles * k_blocks / W blocks against W / tiles partials gives
+// W = tiles * sqrt(0.18 * k_blocks), at most the resident clusters.  (Using
+// every cluster made a 256 x 256 x 65536 product split its one tile 76 ways
+// and spend most of its time in the owner's fix-up.)
+int64_t tail_workers(int64_t tiles, int64_t k_blocks, int64_t slots)
+{
+    int64_t w = int64_t(double(tiles) * sqrt(0.18 * double(k_blocks)) + 0.5);
+    if (w < 1) w = 1;
+    return w < slots ? w : slots;
+}
+
 // Rotation and a stream-K tail exclude each other (the tail does not rotate).
 // Rotation wins where it was measured to (one row or column of tiles filling
 // most of the machine, e.g. 128 x 16384 x 16384); when fewer than half of
@@ -213,6 +230,7 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
 {
     if (layout == 1) return m <= 128 ? 6 : 7;  // B stored [K, N], fp32 result
     if (m <= 128) return 1;
+    if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
     auto slots_of = [&](int v) -> int64_t {
         const int64_t s = slots_by_variant ? slots_by_variant[v] : num_sms / (kVariants[v].cg * kVariants[v].mc);
         return s < 1 ? 1 : s;
@@ -325,8 +343,10 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
         const int64_t full_waves = p.num_tiles / slots;
         const int64_t dp = full_waves >= 1 ? (full_waves - 1) * slots : 0;
         const int64_t sk_iters = (p.num_tiles - dp) * p.k_blocks;
-        if (sk_iters >= slots) {
-            clusters = slots;
+        const int64_t workers = dp == 0 ? tail_workers(p.num_tiles, p.k_blocks, slots) : slots;
+        // with no data-parallel wave left, a tail on no more clusters than tiles would split nothing
+        if (sk_iters >= workers && (dp > 0 || workers > p.num_tiles)) {
+            clusters = workers;
             p.stream_k = 1;
             p.dp_tiles = dp;
             p.sk_iters = sk_iters;

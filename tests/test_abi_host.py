@@ -4,6 +4,7 @@ deterministically, and its scheduler arithmetic (raster map, fast division)
 is exact.  The scheduler functions checked here are the same inline code
 the kernel runs."""
 import ctypes
+import math
 import os
 import re
 
@@ -175,9 +176,14 @@ def test_stream_k_plan_invariants(L, shape, variant):
             assert p.num_tiles - p.dp_tiles <= 2 * workers            # at most two waves are split
             bn = G.gemm_f16_variant_info(variant)["block_n"]        # one CTA's partial tile is 128 x bn
             assert p.workspace_bytes >= p.grid * 128 * bn * 4 + p.grid * 8
-            assert workers == sms // p.cluster
+            slots = sms // p.cluster
+            if p.dp_tiles > 0:                                        # after whole waves: every cluster
+                assert workers == slots
+            else:                                                     # few tiles: sized against the fix-up
+                assert workers == min(slots, max(1, int(p.num_tiles * math.sqrt(0.18 * p.k_blocks) + 0.5)))
+                assert workers > p.num_tiles
         else:                                                         # too little work to split
-            assert p.workspace_bytes == 0 and p.dp_tiles == p.num_tiles and p.num_tiles * p.k_blocks < workers + sms
+            assert p.workspace_bytes == 0 and p.dp_tiles == p.num_tiles
         q = G.gemm_f16_nt_plan_for(m, n, k, sms, 0, variant, 0, 0)
         assert q.stream_k == 0 and q.workspace_bytes == 0 and q.dp_tiles == q.num_tiles
 
