@@ -261,6 +261,28 @@ int64_t streamk_partials_bytes(int64_t grid, int32_t block_n)
     return round_up(grid * 128 * int64_t(block_n) * 4, 256);
 }
 
+// Split-K workspace: one fp32 part of 128 x block_n per CTA of every (tile, part).
+int64_t splitk_workspace_bytes(int64_t tiles, int64_t parts, int32_t cluster, int32_t block_n)
+{
+    return round_up(tiles * parts * cluster * 128 * int64_t(block_n) * 4, 256);
+}
+
+// Split-K needs the fp16 [N,K] layout without operand swap and tiles of whole 64-column chunks.
+bool split_capable(const Variant &var)
+{
+    return var.layout == 0 && !var.swap && var.bn % 64 == 0 && var.bn <= 256;
+}
+
+// Parts per tile: about one (tile, part) per resident cluster, each part at least 4 K blocks; a
+// forced split takes at least 2 parts.  0: no split.
+int64_t split_parts(int64_t tiles, int64_t k_blocks, int64_t slots, bool forced)
+{
+    int64_t s = tiles > 0 ? slots / tiles : 0;
+    if (s > k_blocks / 4) s = k_blocks / 4;
+    if (forced && s < 2) s = k_blocks >= 2 ? 2 : 0;
+    return s >= 2 ? s : 0;
+}
+
 int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
 {
     return streamk_partials_bytes(grid, block_n) + round_up(grid * 8, 256);
@@ -293,7 +315,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     gemm_status_t st = check_shape(m, n, k);
     if (st != GEMM_OK) return st;
     if (num_sms < 1) return GEMM_ERR_INVALID_ARG;
-    if (variant >= kNumVariants || stream_k > 1 || layout > 1) return GEMM_ERR_INVALID_ARG;
+    if (variant >= kNumVariants || stream_k > 2 || layout > 1) return GEMM_ERR_INVALID_ARG;
     if (variant < 0) variant = auto_variant(m, n, cdiv(k, kBlockK), num_sms, slots_by_variant, layout < 0 ? 0 : layout);
     const Variant &var = kVariants[variant];
     if (layout >= 0 && var.layout != layout) return GEMM_ERR_INVALID_ARG;
@@ -353,6 +375,27 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
             p.workspace_bytes = uint64_t(streamk_workspace_bytes(clusters * cs, var.bn));
         }
     }
+    // Split-K instead of a tail that has no whole wave in front of it (fewer tiles than clusters),
+    // or when asked for (stream_k == 2).  Measured on GB300 against the tail sized by tail_workers
+    // (sustained TFLOP/s): 256x256x65536 385 vs 132, 512x512x65536 929 vs 429, 1024x1024x16384
+    // 1051 vs 895, 200x1000x3000 84 vs 60, 1024^3 150 vs 122, 8192x128x8192 493 vs 476: every
+    // split tile's parts are added by the whole GPU instead of one owner after another.
+    p.split_k = 0;
+    if (stream_k == 2 && !split_capable(var)) return GEMM_ERR_INVALID_ARG;
+    const bool split_candidate = stream_k < 0 && split_capable(var) && p.stream_k == 1 && p.dp_tiles == 0;
+    if ((stream_k == 2 || split_candidate) && p.num_tiles > 0) {
+        const int64_t parts = split_parts(p.num_tiles, p.k_blocks, slots, stream_k == 2);
+        if (parts > 1) {
+            const int64_t units = p.num_tiles * parts;
+            clusters = units < slots ? units : slots;
+            p.split_k = int32_t(parts);
+            p.stream_k = 0;
+            p.dp_tiles = p.num_tiles;
+            p.sk_iters = 0;
+            p.k_rotate = 0;
+            p.workspace_bytes = uint64_t(splitk_workspace_bytes(p.num_tiles, parts, cs, var.bn));
+        }
+    }
     p.grid = int32_t(clusters * cs);
     if (raster_width <= 0) raster_width = auto_raster_width(p.tiles_n, p.block_n);
     if (p.tiles_n > 0 && raster_width > p.tiles_n) raster_width = int32_t(p.tiles_n);
@@ -393,7 +436,17 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         return GEMM_ERR_INVALID_ARG;
     const int64_t workers = plan.grid / plan.cluster;
     if (plan.k_rotate != 0 && plan.k_rotate != 1) return GEMM_ERR_INVALID_ARG;
-    if (plan.stream_k == 0) {
+    if (plan.split_k > 1) {
+        // clusters walk the (tile, part) units persistently and wait for nobody: any grid works
+        if (plan.stream_k != 0 || !split_capable(kVariants[plan.variant]) || plan.dp_tiles != plan.num_tiles ||
+            plan.sk_iters != 0 || plan.split_k > plan.k_blocks || workers > plan.num_tiles * plan.split_k ||
+            int64_t(plan.workspace_bytes) !=
+                splitk_workspace_bytes(plan.num_tiles, plan.split_k, plan.cluster, kVariants[plan.variant].bn))
+            return GEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
+    } else if (plan.split_k != 0 && plan.split_k != 1) {
+        return GEMM_ERR_INVALID_ARG;
+    } else if (plan.stream_k == 0) {
         // any grid of whole clusters is correct: the kernel walks the tiles persistently
         if (plan.dp_tiles != plan.num_tiles || plan.sk_iters != 0 || workers > plan.num_tiles)
             return GEMM_ERR_INVALID_ARG;
@@ -424,6 +477,10 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     params.dp_tiles = uint32_t(plan.dp_tiles);
     params.k_rotate = plan.k_rotate ? 1u : 0u;
     params.sk_iters = uint64_t(plan.sk_iters);
+    if (plan.split_k > 1) {
+        params.split_k = uint32_t(plan.split_k);
+        params.partials = static_cast<float *>(ws);
+    }
     if (plan.stream_k) {
         params.partials = static_cast<float *>(ws);
         params.flags = reinterpret_cast<uint64_t *>(static_cast<char *>(ws) +
@@ -439,6 +496,10 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     }
     params.error_word = static_cast<uint32_t *>(err_ptr);
     if (var.launch(plan, params, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    if (plan.split_k > 1 && launch_split_reduce(plan, var, params.raster, ws, c, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }

@@ -99,7 +99,8 @@ struct KernelParams {
     uint32_t dp_tiles;    // tiles [0, dp_tiles) are walked data-parallel
     uint32_t k_rotate;    // 1: a whole tile starts its K walk at a per-tile offset (see the producer)
     uint64_t sk_iters;    // K iterations of tiles [dp_tiles, num_tiles), split evenly over the clusters
-    float *partials;      // stream-K workspace: one 128 x BN fp32 partial tile per CTA
+    uint32_t split_k;     // > 1: split-K, tile t's K blocks cut into split_k parts, each published
+    float *partials;      // stream-K workspace: one 128 x BN fp32 partial tile per CTA (split-K: per part and CTA)
     uint64_t *flags;      // stream-K workspace: one "partial published" stamp per CTA
     uint64_t sk_stamp;    // this launch's stamp: a flag equal to it marks a partial of this launch
     uint32_t skip_fill;   // test hook: k-block fill (counted across CTA 0's tiles) the producer
@@ -218,11 +219,22 @@ __device__ __forceinline__ uint64_t sk_begin(const KernelParams &p, uint32_t w, 
 }
 
 // Every role walks the same sequence of segments (tile, [k_lo, k_hi)):
-// data-parallel tiles first, then this cluster's stream-K range.  f returns
-// false to stop early (abort).
+// data-parallel tiles first, then this cluster's stream-K range; with split-K
+// instead the parts u = tile * split_k + s, s-th of split_k equal K ranges,
+// one after another per cluster.  f returns false to stop early (abort).
 template <class F>
 __device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t worker, uint32_t workers, F &&f)
 {
+    if (p.split_k > 1) {
+        const uint64_t units = uint64_t(p.num_tiles) * p.split_k;
+        for (uint64_t u = worker; u < units; u += workers) {
+            const uint32_t tile = uint32_t(u / p.split_k), part = uint32_t(u % p.split_k);
+            const uint32_t k_lo = uint32_t(uint64_t(part) * p.k_blocks / p.split_k);
+            const uint32_t k_hi = uint32_t(uint64_t(part + 1) * p.k_blocks / p.split_k);
+            if (!f(tile, k_lo, k_hi)) return;
+        }
+        return;
+    }
     for (uint32_t tile = worker; tile < p.dp_tiles; tile += workers)
         if (!f(tile, 0u, p.k_blocks)) return;
     if (p.sk_iters == 0) return;
@@ -449,9 +461,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                                             : mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u + quarter * 32u;
             const uint32_t col0 = Cfg::kAMC ? (nb * MC + cta_rank) * BN : nb * BN;
             const bool ok = wait_bounded<CS>(bar_acc_full(acc), acc_phase, p, abort_flag, kErrWaitAccFull);
-            // A split tile meets the other epilogue warps at named barrier 1 below, so the decision
-            // to stop must be the same in all four warps; a whole tile needs it per warp only.
-            const bool split = (k_lo != 0) || (k_hi != p.k_blocks);
+            // A stream-K split tile meets the other epilogue warps at named barrier 1 below, so the
+            // decision to stop must be the same in all four warps; otherwise it is per warp.
+            const bool split = (p.split_k <= 1) && ((k_lo != 0) || (k_hi != p.k_blocks));
             const bool all_ok = split ? ptx::named_barrier_and(1, 32 * kEpiWarps, ok) : __all_sync(0xffffffffu, ok);
             if (!all_ok) return false;
             ptx::tc_fence_after_sync();
@@ -459,9 +471,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             // Partial-tile layout in the workspace: per warp quarter and 64-column chunk, 16 float4
             // slots x 32 lanes, so every warp-wide 16-byte access is one contiguous 512-byte run.
             const uint32_t piece = quarter * 32u * BN + lane * 4u;
-            if (k_lo != 0) {
-                // ---- publish this partial tile; the owner of the tile adds it
-                float *slot = p.partials + size_t(blockIdx.x) * kSlotFloats + piece;
+            if (p.split_k > 1 || k_lo != 0) {
+                // ---- publish this partial tile: a split-K part to its own slot (the reduction
+                // kernel adds the parts), a stream-K part for the owner of the tile to add.  Part s
+                // of tile t starts at floor(s * k_blocks / split_k), so s = ceil(k_lo * split_k / k_blocks)
+                // (split_k <= k_blocks)
+                size_t slot_index = blockIdx.x;
+                if (p.split_k > 1) {
+                    const uint64_t part = (uint64_t(k_lo) * p.split_k + p.k_blocks - 1) / p.k_blocks;
+                    slot_index = (uint64_t(tile) * p.split_k + part) * CS + cta_rank;
+                }
+                float *slot = p.partials + slot_index * kSlotFloats + piece;
                 if (row0 < p.m) {
                     auto publish = [&](auto width, int c) {
                         constexpr int W = decltype(width)::value;
@@ -480,9 +500,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     for (int c = 0; c < Cfg::kFullChunks; ++c) publish(std::integral_constant<int, 64>{}, c);
                     if constexpr (Cfg::kTail) publish(std::integral_constant<int, 32>{}, Cfg::kFullChunks);
                 }
-                __threadfence();
-                ptx::named_barrier_sync(1, 32 * kEpiWarps);
-                if (first_epi_thread) ptx::st_release_gpu_u64(p.flags + blockIdx.x, p.sk_stamp);
+                if (p.split_k <= 1) {
+                    __threadfence();
+                    ptx::named_barrier_sync(1, 32 * kEpiWarps);
+                    if (first_epi_thread) ptx::st_release_gpu_u64(p.flags + blockIdx.x, p.sk_stamp);
+                }
             } else {
                 // ---- a whole tile, or the owning segment of a split tile
                 uint32_t first_w = 0, last_w = 0;  // contributors [first_w, last_w)
@@ -632,6 +654,59 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     else __syncthreads();
     ptx::tc_fence_after_sync();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+}
+
+// Split-K reduction: for every tile, adds its split_k fp32 parts in part
+// order and writes the fp16 result (round to nearest even) to C.  The parts
+// use the epilogue's publish layout: per CTA, 128 x bn floats in which float4
+// number i = (q * bn / 4 + c * 16 + j) * 32 + lane holds row 32 q + lane of
+// the CTA's rows and columns 64 c + 4 j .. + 3 of its columns.  One thread per
+// float4; rows at or past M and columns at or past N are skipped (the
+// epilogue never wrote them), so C outside [0, M) x [0, N) is untouched.
+struct SplitReduceParams {
+    const float *parts;
+    __half *c;
+    Raster raster;
+    uint32_t m, n;
+    uint32_t split_k;
+    uint32_t bn;          // columns of one CTA's part (multiple of 64)
+    uint32_t cs;          // CTAs per cluster (parts per tile and split)
+    uint32_t block_m;     // rows of a cluster tile
+    uint32_t block_n;     // columns of a cluster tile
+    uint32_t cta_rows;    // row offset between the CTAs of a cluster (128, or 0 when they sit along N)
+    uint64_t threads;     // num_tiles * cs * 32 * bn
+};
+
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ SplitReduceParams p)
+{
+    const uint64_t g = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (g >= p.threads) return;
+    const uint64_t per_cta = 32ull * p.bn;  // float4s in one CTA's part
+    const uint32_t i = uint32_t(g % per_cta);
+    const uint32_t cta = uint32_t((g / per_cta) % p.cs);
+    const uint32_t tile = uint32_t(g / (per_cta * p.cs));
+    const uint32_t lane = i & 31u, r = i >> 5;
+    const uint32_t q = r / (p.bn / 4u), rr = r % (p.bn / 4u);
+    const uint32_t chunk = rr / 16u, j = rr % 16u;
+    uint32_t mb, nb;
+    raster_coord(p.raster, tile, mb, nb);
+    const uint32_t row = mb * p.block_m + (p.cta_rows ? cta * p.cta_rows : 0u) + q * 32u + lane;
+    const uint32_t col = nb * p.block_n + (p.cta_rows ? 0u : cta * p.bn) + chunk * 64u + j * 4u;
+    if (row >= p.m || col >= p.n) return;  // n % 8 == 0, col % 4 == 0: the whole float4 is inside
+    const float4 *src = reinterpret_cast<const float4 *>(p.parts) + (uint64_t(tile) * p.split_k * p.cs + cta) * per_cta + i;
+    float4 acc = src[0];
+    for (uint32_t s = 1; s < p.split_k; ++s) {
+        const float4 v = src[uint64_t(s) * p.cs * per_cta];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    const __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+    uint2 out;
+    out.x = *reinterpret_cast<const uint32_t *>(&lo);
+    out.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p.c + uint64_t(row) * p.n + col) = out;
 }
 
 }  // namespace gemm_f16

@@ -195,4 +195,27 @@ gemm_status_t encode_tensor_maps(const Variant &var, const gemm_f16_plan_t &plan
     return GEMM_OK;
 }
 
+// The split-K reduction of a plan with split_k > 1, after its GEMM launch on the same stream.
+cudaError_t launch_split_reduce(const gemm_f16_plan_t &plan, const Variant &var, const Raster &raster,
+                                const void *parts, void *c, cudaStream_t stream)
+{
+    SplitReduceParams r;
+    memset(&r, 0, sizeof(r));
+    r.parts = static_cast<const float *>(parts);
+    r.c = static_cast<__half *>(c);
+    r.raster = raster;
+    r.m = uint32_t(plan.m);
+    r.n = uint32_t(plan.n);
+    r.split_k = uint32_t(plan.split_k);
+    r.bn = uint32_t(var.bn);
+    r.cs = uint32_t(var.cg * var.mc);
+    r.block_m = uint32_t(plan.block_m);
+    r.block_n = uint32_t(plan.block_n);
+    r.cta_rows = (var.cg == 1 && var.mc > 1) ? 0u : 128u;  // single CTAs sharing A sit along N
+    r.threads = uint64_t(plan.num_tiles) * r.cs * 32u * r.bn;
+    const uint64_t blocks = (r.threads + 255u) / 256u;
+    splitk_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(r);
+    return cudaGetLastError();
+}
+
 }  // namespace gemm_f16

@@ -60,6 +60,7 @@ class Plan(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("num_sms", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_uint64),
+        ("split_k", ctypes.c_int32),
     ]
 
     def as_dict(self):

@@ -95,6 +95,7 @@ typedef struct gemm_f16_plan {
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t num_sms;         /* SM count the plan was made for */
     uint64_t workspace_bytes;/* device workspace the plan needs (0 = none) */
+    int32_t split_k;         /* 0: off; S > 1: split-K, each tile's K range cut into S parts (below) */
 } gemm_f16_plan_t;
 
 /*
@@ -114,6 +115,18 @@ typedef struct gemm_f16_plan {
  * of split tiles only within the fp32 accumulation error.  The 256 x 512
  * tile (block_n 512) has no stream-K tail: asking for one is
  * GEMM_ERR_INVALID_ARG, and automatic plans never give it one.
+ *
+ * Split-K ("split_k == S > 1", stream_k 0): for products with fewer tiles
+ * than resident clusters and a long K.  Each tile's K blocks are cut into S
+ * equal contiguous parts; the clusters compute the tiles x S parts
+ * independently and write each fp32 part to its own workspace slot (no
+ * flags, no waiting between clusters); a second kernel, launched on the same
+ * stream right after, adds a tile's S parts in a fixed order and writes the
+ * fp16 result.  Workspace: tiles x S x (CTAs per cluster) parts of
+ * 128 x block_n fp32.  Unlike the stream-K tail, no one cluster adds many
+ * parts, so a tile's K can be spread over the whole GPU.  Variants with
+ * fp16 C, B [N,K], tiles of whole 64-column chunks and no operand swap only
+ * (0-4, 11, 12).
  */
 
 /* Human-readable name of a status code (static string, never NULL). */

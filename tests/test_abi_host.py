@@ -254,17 +254,20 @@ def test_k_rotation_rule(L):
     assert big.k_rotate == 0                                   # strips shared by neighbouring tiles
 
 
-@pytest.mark.parametrize("shape,variant,stream_k", [
-    ((8192, 8192, 8192), 15, 0),     # 256 x 512 pair tiles: least data per flop, 96% of the waves busy
-    ((6144, 6144, 6144), 15, 0),
-    ((4096, 8192, 4096), 2, 0),      # 256 x 256 pair tiles fill 96% of their waves, the wide ones 84%
-    ((3000, 5000, 4096), 4, 1),      # multicast pairs with a stream-K tail beat a 79%-busy wide tile
-    ((256, 256, 256), 2, 0),         # one tile: the wide tile would compute twice the area
-    ((128, 16384, 16384), 1, 0),     # M <= 128: single-CTA 128 x 128 tiles, rotated K walk
-    ((256, 256, 1 << 20), 2, 1),     # one tile: its K is split over every cluster instead of rotated
+@pytest.mark.parametrize("shape,variant,stream_k,split", [
+    ((8192, 8192, 8192), 15, 0, False),    # 256 x 512 pair tiles: least data per flop, 96% of the waves busy
+    ((6144, 6144, 6144), 15, 0, False),
+    ((4096, 8192, 4096), 2, 0, False),     # 256 x 256 pair tiles fill 96% of their waves, the wide ones 84%
+    ((3000, 5000, 4096), 4, 1, False),     # multicast pairs with a stream-K tail beat a 79%-busy wide tile
+    ((256, 256, 256), 2, 0, False),        # one tile: the wide tile would compute twice the area
+    ((128, 16384, 16384), 1, 0, False),    # M <= 128: single-CTA 128 x 128 tiles, rotated K walk
+    ((256, 256, 1 << 20), 2, 0, True),     # one tile, long K: split-K over every cluster
+    ((512, 512, 65536), 4, 0, True),
+    ((200, 1000, 3000), 2, 0, True),       # few tiles: split-K rather than a tail without a whole wave
+    ((4096, 4096, 4096), 4, 1, False),     # whole waves in front: a stream-K tail over every cluster
 ])
-def test_auto_variant_choices(L, shape, variant, stream_k):
+def test_auto_variant_choices(L, shape, variant, stream_k, split):
     """The automatic plan's tile choice on a 152-SM part with every variant's full complement of
-    clusters (the measured cases its cost estimate was fitted to)."""
+    clusters (the measured cases its cost estimates were fitted to)."""
     p = G.gemm_f16_nt_plan_for(*shape, 152)
-    assert (p.variant, p.stream_k) == (variant, stream_k)
+    assert (p.variant, p.stream_k, p.split_k > 1) == (variant, stream_k, split)

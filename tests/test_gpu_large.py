@@ -1,7 +1,7 @@
 """Parity at the size extremes, through the automatic plan: a C of 2^32
 elements (8 GiB; element offsets past 32 bits), 2^20 rows of one 8-column
 strip (4096 tile rows), and K = 2^20 on one output tile (16384 K blocks, so
-the stream-K tail splits a single tile's K over every cluster).  Operands in
+split-K cuts that tile's K into parts over every cluster).  Operands in
 {-8..8}/8 make every product a multiple of 2^-6, so fp32 sums are exact while
 their partial sums stay below 2^18 in magnitude: always for K = 64, and for
 K = 2^20 because these zero-mean draws keep them in the hundreds.  So the
@@ -69,5 +69,5 @@ def test_one_strip_of_2_pow_20_rows():
 def test_k_of_2_pow_20_on_one_tile(ws):
     p = G.gemm_f16_nt_plan(256, 256, 1 << 20)
     if ws:
-        assert p.stream_k == 1                  # the one tile's K is split over all clusters
+        assert p.split_k > 1                    # the one tile's K is split over all clusters
     _check_sampled(256, 256, 1 << 20, 300, seed=43, ws=ws)
