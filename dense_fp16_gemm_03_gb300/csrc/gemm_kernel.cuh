@@ -221,11 +221,12 @@ __device__ __forceinline__ uint64_t sk_begin(const KernelParams &p, uint32_t w, 
 // Every role walks the same sequence of segments (tile, [k_lo, k_hi)):
 // data-parallel tiles first, then this cluster's stream-K range; with split-K
 // instead the parts u = tile * split_k + s, s-th of split_k equal K ranges,
-// one after another per cluster.  f returns false to stop early (abort).
-template <class F>
+// one after another per cluster.  f returns false to stop early (abort).  A kernel that never runs
+// split-K plans instantiates it with kSplitK = false.
+template <bool kSplitK = true, class F>
 __device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t worker, uint32_t workers, F &&f)
 {
-    if (p.split_k > 1) {
+    if (kSplitK && p.split_k > 1) {
         const uint64_t units = uint64_t(p.num_tiles) * p.split_k;
         for (uint64_t u = worker; u < units; u += workers) {
             const uint32_t tile = uint32_t(u / p.split_k), part = uint32_t(u % p.split_k);

@@ -23,8 +23,8 @@
 //               and accumulator half (w - 2) / 4, i.e. a 32 x 256 piece.
 //
 // The pipeline, the raster order, the K rotation, the ragged-edge rules and
-// the bounded waits are those of gemm_kernel.cuh; this variant has no
-// stream-K tail (its plans are always data-parallel).
+// the bounded waits are those of gemm_kernel.cuh; this variant has neither a
+// stream-K tail nor split-K (its plans are always data-parallel).
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, fills = 0;
             bool ok = true;
-            for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
+            for_each_segment<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
                 uint32_t mb, nb;
                 raster_coord(p.raster, tile, mb, nb);
                 const int32_t m0 = int32_t(mb * Cfg::kBM + pair_rank * 128u);
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         if (leader && lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(Cfg::kBM, Cfg::kHalfN);
             uint32_t stage = 0, phase = 0, acc_phase = 0;
-            for_each_segment(p, cluster_id, num_clusters, [&](uint32_t, uint32_t k_lo, uint32_t k_hi) {
+            for_each_segment<false>(p, cluster_id, num_clusters, [&](uint32_t, uint32_t k_lo, uint32_t k_hi) {
                 if (!wait_bounded<CS>(bar_acc_empty, acc_phase ^ 1u, p, abort_flag, kErrWaitAccEmpty)) return false;
                 ptx::tc_fence_after_sync();
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb) {
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         const uint32_t row_addr = buf + lane * 128u;
         const uint32_t t_col = tmem_base + ((quarter * 32u) << 16) + half * uint32_t(Cfg::kHalfN);
         uint32_t acc_phase = 0;
-        for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
+        for_each_segment<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
             const uint32_t row0 = mb * Cfg::kBM + pair_rank * 128u + quarter * 32u;
