@@ -261,6 +261,11 @@ int64_t streamk_partials_bytes(int64_t grid, int32_t block_n)
     return round_up(grid * 128 * int64_t(block_n) * 4, 256);
 }
 
+int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
+{
+    return streamk_partials_bytes(grid, block_n) + round_up(grid * 8, 256);
+}
+
 // Split-K workspace: one fp32 part of 128 x block_n per CTA of every (tile, part).
 int64_t splitk_workspace_bytes(int64_t tiles, int64_t parts, int32_t cluster, int32_t block_n)
 {
@@ -281,11 +286,6 @@ int64_t split_parts(int64_t tiles, int64_t k_blocks, int64_t slots, bool forced)
     if (s > k_blocks / 4) s = k_blocks / 4;
     if (forced && s < 2) s = k_blocks >= 2 ? 2 : 0;
     return s >= 2 ? s : 0;
-}
-
-int64_t streamk_workspace_bytes(int64_t grid, int32_t block_n)
-{
-    return streamk_partials_bytes(grid, block_n) + round_up(grid * 8, 256);
 }
 
 // Stamps of stream-K launches: a per-process random high word and a counter,

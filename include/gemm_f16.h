@@ -156,8 +156,9 @@ gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t 
  * Plan for a device with `num_sms` SMs (and `max_clusters` co-resident
  * 2-CTA clusters, or 0 for num_sms / 2) without touching any device.
  * `variant` < 0 picks automatically; `raster_width` <= 0 picks
- * automatically; `stream_k` < 0 picks automatically, 0 forbids and 1
- * requests the stream-K tail.  Pure host code: it is the planning logic the
+ * automatically; `stream_k` < 0 picks automatically (stream-K tail or
+ * split-K where they pay), 0 forbids both, 1 requests the stream-K tail and
+ * 2 requests split-K (GEMM_ERR_INVALID_ARG for a variant without it).  Pure host code: it is the planning logic the
  * device entry points use, exposed for inspection and tests.
  */
 gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_sms,
