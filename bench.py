@@ -463,7 +463,7 @@ def main():
         "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
         "frac_of_nominal_peak": value / world / NOMINAL_PEAK_TFLOPS,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if plan.split_k > 1 else 1),  # a split-K plan adds its reduction
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

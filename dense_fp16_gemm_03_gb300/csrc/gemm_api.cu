@@ -444,6 +444,9 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
                 splitk_workspace_bytes(plan.num_tiles, plan.split_k, plan.cluster, kVariants[plan.variant].bn))
             return GEMM_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
+        // the reduction runs one thread per float4 of every part: its grid must fit the launch limit
+        const int64_t reduce_blocks = cdiv(plan.num_tiles * plan.cluster * 32 * kVariants[plan.variant].bn, 256);
+        if (reduce_blocks > 0x7FFFFFFF) return GEMM_ERR_UNSUPPORTED_SHAPE;
     } else if (plan.split_k != 0 && plan.split_k != 1) {
         return GEMM_ERR_INVALID_ARG;
     } else if (plan.stream_k == 0) {
