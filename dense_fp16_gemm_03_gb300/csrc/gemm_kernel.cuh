@@ -680,6 +680,10 @@ struct SplitReduceParams {
 
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ SplitReduceParams p)
 {
+    // Launched as a programmatic dependent of the GEMM that wrote the parts: blocks may start on SMs
+    // the GEMM has left, and wait here until that whole grid has completed and its writes are visible.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     const uint64_t g = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (g >= p.threads) return;
     const uint64_t per_cta = 32ull * p.bn;  // float4s in one CTA's part

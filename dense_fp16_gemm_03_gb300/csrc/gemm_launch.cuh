@@ -213,9 +213,18 @@ cudaError_t launch_split_reduce(const gemm_f16_plan_t &plan, const Variant &var,
     r.block_n = uint32_t(plan.block_n);
     r.cta_rows = (var.cg == 1 && var.mc > 1) ? 0u : 128u;  // single CTAs sharing A sit along N
     r.threads = uint64_t(plan.num_tiles) * r.cs * 32u * r.bn;
-    const uint64_t blocks = (r.threads + 255u) / 256u;
-    splitk_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(r);
-    return cudaGetLastError();
+    const uint64_t blocks = (r.threads + 255u) / 256u;  // within the grid limit (run_plan checks)
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the GEMM's tail
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, r);
 }
 
 }  // namespace gemm_f16
