@@ -198,30 +198,42 @@ int64_t tail_workers(int64_t tiles, int64_t k_blocks, int64_t slots)
 
 // Rotation and a stream-K tail exclude each other (the tail does not rotate).
 // Rotation wins where it was measured to (one row or column of tiles filling
-// most of the machine, e.g. 128 x 16384 x 16384); when fewer than half of
-// the slots would have a tile (e.g. one 256 x 256 tile with K = 2^20), only
-// splitting K over the clusters keeps the machine busy, so the tail wins.
+// most of one wave, e.g. 128 x 16384 x 16384); when fewer than half of the
+// slots would have a tile (e.g. one 256 x 256 tile with K = 2^20), only
+// splitting K over the clusters keeps the machine busy, and when the tiles
+// spill into a second, partial wave (157 tiles of 128 x 128 for 152 SMs:
+// 100 x 20000 x 8192), the few clusters of that wave would run alone for a
+// whole tile, so the tail wins.
 void tail_choice(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks, int64_t slots, bool *rotate, bool *stream_k)
 {
     const int64_t tiles = tiles_m * tiles_n;
     const bool sk = streamk_pays(tiles, k_blocks, slots);
-    *rotate = rotate_pays(tiles_m, tiles_n, k_blocks) && !(sk && wave_efficiency(tiles, slots) < 0.5);
+    *rotate = rotate_pays(tiles_m, tiles_n, k_blocks) && !(sk && (wave_efficiency(tiles, slots) < 0.5 || tiles > slots));
     *stream_k = sk && !*rotate;
 }
 
 // Tile-shape choice, from interleaved measurements on GB300 under the power
 // cap:
-//  - M <= 128: one 128-row tile; a CTA pair's second CTA would idle, the
-//    single-CTA 128 x 128 tile (variant 1) is fastest;
-//  - otherwise the cheaper of the 256 x 512 pair tile (variant 15) and an
-//    alternative with 256-column tiles: the 256 x 256 pair tile (variant 2)
-//    for M <= 256 or when its waves keep >= 95% of the pair slots busy,
-//    else two pairs sharing B by multicast (variant 4, whole clusters of
-//    four SMs only).
+//  - M <= 128: one 128-row tile of A.  With enough rows of B to give at
+//    least half the CTA pairs a tile, the swapped pair tile (variant 13:
+//    256 rows of B on the MMA's M side, A's 128 rows on N) brings 24 KB per
+//    K block into each SM against 32 KB for the single-CTA 128 x 128 tile
+//    (variant 1), measured +0.5 to +4% on products that stream B from HBM
+//    (128 x 16384 x 16384: 785 against 767 TFLOP/s; -0.7 to -1.4% on two
+//    with K = 4096); with fewer, variant 1, whose K can be split;
+//  - otherwise the cheapest of the wide pair tiles, 256 x 512 (variant 15)
+//    and 256 x 448 (variant 16), and an alternative with 256-column tiles:
+//    the 256 x 256 pair tile (variant 2) for M <= 256 or when its waves keep
+//    >= 95% of the pair slots busy, else two pairs sharing B by multicast
+//    (variant 4, whole clusters of four SMs only).
 // The estimate is waves x work per SM in units of a 256 x 256 pair tile
 // (variants 2 and 4: 1 per tile).  A 256 x 512 tile is 2 units but moves 25%
 // less data per flop, which under the power cap bought ~6% more clock
-// (8192^3: +4-5%); it counts 1.88.  An alternative whose tail stream-K
+// (8192^3: +4-5%); it counts 1.88.  A 256 x 448 tile counts 1.69 (8192^3:
+// 8 of its waves ran 3% longer than 7 of the 512-column ones); it pays where
+// N / 512 leaves the last wave mostly idle and N / 448 fills it
+// (3000 x 5000 x 4096: 1486 against 1433 TFLOP/s; 4096 x 8192 x 4096: 1581
+// against 1573 for the 256 x 256 tile).  An alternative whose tail stream-K
 // balances counts its tiles / slots plus 3% for the fix-up.  This picked
 // the faster plan on 12 of 13 measured shapes (4096^3, 8192^3, 6144^3,
 // 3000 x 5000 x 4096, 4096 x 8192 x 4096, ...; the miss, 7168^3, by 0.7%).
@@ -229,12 +241,12 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
                      int32_t layout)
 {
     if (layout == 1) return m <= 128 ? 6 : 7;  // B stored [K, N], fp32 result
-    if (m <= 128) return 1;
-    if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
     auto slots_of = [&](int v) -> int64_t {
         const int64_t s = slots_by_variant ? slots_by_variant[v] : num_sms / (kVariants[v].cg * kVariants[v].mc);
         return s < 1 ? 1 : s;
     };
+    if (m <= 128) return 2 * cdiv(n, 256) >= slots_of(13) ? 13 : 1;
+    if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
     const int64_t pair_tiles_m = cdiv(m, 256), tiles_n = cdiv(n, 256);
     int32_t alt = 2;
     int64_t alt_tiles_m = pair_tiles_m;
@@ -246,8 +258,17 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
     bool alt_rotate = false, alt_sk = false;
     tail_choice(alt_tiles_m, tiles_n, k_blocks, alt_slots, &alt_rotate, &alt_sk);
     const double alt_cost = alt_sk ? 1.03 * double(alt_tiles) / double(alt_slots) : double(cdiv(alt_tiles, alt_slots));
-    const double wide_cost = 1.88 * double(cdiv(pair_tiles_m * cdiv(n, 512), slots_of(15)));
-    return wide_cost < alt_cost ? 15 : alt;
+    int32_t best = alt;
+    double best_cost = alt_cost;
+    for (int32_t v : {15, 16}) {  // on a tie the 512-column tile (fewer, fuller tiles) stays
+        const double per_wave = v == 15 ? 1.88 : 1.69;
+        const double cost = per_wave * double(cdiv(pair_tiles_m * cdiv(n, kVariants[v].bn), slots_of(v)));
+        if (cost < best_cost) {
+            best = v;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 int64_t round_up(int64_t x, int64_t a)
@@ -351,7 +372,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.sk_iters = 0;
     p.workspace_bytes = 0;
     // the wide variant has no stream-K tail: asking for one is an error, the automatic choice skips it
-    const bool sk_capable = var.bn <= 256;
+    const bool sk_capable = !is_wide(var);
     if (stream_k == 1 && !sk_capable) return GEMM_ERR_INVALID_ARG;
     // rotation or a stream-K tail (tail_choice); with the tail forbidden or unavailable, rotation alone
     bool rotate = false, tail = false;
@@ -366,8 +387,11 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
         const int64_t dp = full_waves >= 1 ? (full_waves - 1) * slots : 0;
         const int64_t sk_iters = (p.num_tiles - dp) * p.k_blocks;
         const int64_t workers = dp == 0 ? tail_workers(p.num_tiles, p.k_blocks, slots) : slots;
-        // with no data-parallel wave left, a tail on no more clusters than tiles would split nothing
-        if (sk_iters >= workers && (dp > 0 || workers > p.num_tiles)) {
+        // the tail must shorten the longest cluster's work: data-parallel, the tail's tiles take
+        // ceil(left / min(left, slots)) tiles on some cluster; the tail gives each left / workers
+        const int64_t left = p.num_tiles - dp;
+        const int64_t dp_waves = cdiv(left, left < slots ? left : slots);
+        if (sk_iters >= workers && left < dp_waves * workers) {
             clusters = workers;
             p.stream_k = 1;
             p.dp_tiles = dp;
@@ -455,7 +479,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
             return GEMM_ERR_INVALID_ARG;
     } else {
         // owners wait for contributors: every cluster must be resident at once
-        if (plan.stream_k != 1 || kVariants[plan.variant].bn > 256 || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
+        if (plan.stream_k != 1 || is_wide(kVariants[plan.variant]) || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
             plan.sk_iters != (plan.num_tiles - plan.dp_tiles) * plan.k_blocks || plan.sk_iters < workers ||
             workers > dev->max_clusters[plan.variant] ||
             int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, kVariants[plan.variant].bn))

@@ -1,6 +1,7 @@
 // Wide-tile variant of the persistent sm_103a kernel: a CTA pair computes a
-// 256 x 512 tile of C[M,N] = A[M,K] . B[N,K]^T (fp16 in, fp32 accumulate,
-// fp16 out) as two cta_group::2 MMAs of N = 256 per K step.
+// 256 x (2 HALF_N) tile of C[M,N] = A[M,K] . B[N,K]^T (fp16 in, fp32
+// accumulate, fp16 out) as two cta_group::2 MMAs of N = HALF_N per K step
+// (HALF_N = 256: 256 x 512 tiles; 224: 256 x 448).
 //
 // Why a wider tile: every byte of A and B reaches a CTA's shared memory
 // through the SM's port on the L2 crossbar.  On GB300 that delivery measured
@@ -9,18 +10,23 @@
 // A 256 x 256 pair tile brings in (128 + 128) x 128 bytes per K block for
 // 2 x 128 x 256 x 64 flops per SM (128 flop/byte); a 256 x 512 tile brings in
 // (128 + 256) x 128 bytes for twice the flops (171 flop/byte), 25% less
-// crossbar traffic per flop.  The accumulator then fills all 512 tensor-
-// memory columns, so there is no second buffer for the epilogue to drain
-// while the next tile accumulates; instead the epilogue empties tensor
+// crossbar traffic per flop.  The accumulator then fills the tensor memory
+// (half h at column 256 h), so there is no second buffer for the epilogue to
+// drain while the next tile accumulates; instead the epilogue empties tensor
 // memory into registers (converted to fp16) at once, releases it to the MMA
 // warp, and only then writes the tile out through shared memory and TMA.
+// The 448-column form trades 5% of that intensity for wave quantization:
+// where N / 512 leaves the last wave of tiles mostly idle, N / 448 can fill
+// it (3000 x 5000: 144 tiles for 152 SMs instead of 120).
 //
 // Roles (320 threads):
-//   warp 0      TMA producer: per K block, A (128 rows) and two 128-row B
-//               sub-tiles per CTA into a STAGES-deep ring (48 KB a stage).
+//   warp 0      TMA producer: per K block, A (128 rows) and two HALF_N / 2-row
+//               B sub-tiles per CTA into a STAGES-deep ring.
 //   warp 1      MMA issuer of the pair (first CTA) and tensor-memory owner.
 //   warps 2..9  epilogue: warp w reads tensor-memory lanes [32 (w mod 4), +32)
-//               and accumulator half (w - 2) / 4, i.e. a 32 x 256 piece.
+//               and accumulator half (w - 2) / 4, i.e. a 32 x HALF_N piece,
+//               stored as 64-column boxes and, when HALF_N mod 64 = 32, one
+//               last 32-column box.
 //
 // The pipeline, the raster order, the K rotation, the ragged-edge rules and
 // the bounded waits are those of gemm_kernel.cuh; this variant has neither a
@@ -34,15 +40,19 @@ namespace gemm_f16 {
 constexpr int kWideEpiWarps = 8;
 constexpr int kWideThreads = 64 + 32 * kWideEpiWarps;
 
-template <int STAGES>
+template <int STAGES, int HALF_N>
 struct WideCfg {
-    static constexpr int kBN = 512;                       // tile columns: two MMAs of N = 256
-    static constexpr int kHalfN = 256;
+    static_assert(HALF_N % 32 == 0 && HALF_N >= 128 && HALF_N <= 256, "one MMA's N: whole 32-column chunks");
+    static constexpr int kHalfN = HALF_N;                 // columns per MMA
+    static constexpr int kBN = 2 * HALF_N;                // tile columns: two MMAs
     static constexpr int kBM = 256;                       // tile rows: the pair's MMA M
+    static constexpr int kHalfCol = 256;                  // tensor-memory column of accumulator half 1
+    static constexpr int kFullChunks = HALF_N / 64;       // 64-column epilogue chunks per half
+    static constexpr bool kTail = (HALF_N % 64) != 0;     // plus one 32-column chunk
     static constexpr int kABytes = 128 * kBlockK * 2;     // one CTA's 128 rows of A
-    static constexpr int kBSubBytes = 128 * kBlockK * 2;  // one 128-row B sub-tile
+    static constexpr int kBBoxRows = HALF_N / 2;          // the rank's share of one MMA's B rows
+    static constexpr int kBSubBytes = kBBoxRows * kBlockK * 2;
     static constexpr int kBBytes = 2 * kBSubBytes;
-    static constexpr int kBBoxRows = 128;
     static constexpr int kStageTx = (kABytes + kBBytes) * 2;  // both CTAs' bytes land on the leader's barrier
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
@@ -54,6 +64,8 @@ struct WideCfg {
     static constexpr int kSmemUsed = kOffAbort + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kTmemCols = 512;
+    static_assert(kBSubBytes % 1024 == 0, "B sub-tiles stay 1024-byte aligned for the 128-byte swizzle");
+    static_assert(kHalfCol + kHalfN <= kTmemCols, "both accumulator halves fit tensor memory");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
 
@@ -67,10 +79,10 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t row_addr, uint32_t row,
                           w[4 * j + 3]);
 }
 
-template <int STAGES>
+template <int STAGES, int HALF_N>
 __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = WideCfg<STAGES>;
+    using Cfg = WideCfg<STAGES, HALF_N>;
     constexpr int CS = 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -105,6 +117,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         ptx::prefetch_tmap(&p.tmap_a);
         ptx::prefetch_tmap(&p.tmap_b);
         ptx::prefetch_tmap(&p.tmap_c);
+        if constexpr (Cfg::kTail) ptx::prefetch_tmap(&p.tmap_c32);
     }
     if (warp == 1) {
         ptx::tmem_alloc<2>(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
@@ -126,8 +139,9 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                 uint32_t mb, nb;
                 raster_coord(p.raster, tile, mb, nb);
                 const int32_t m0 = int32_t(mb * Cfg::kBM + pair_rank * 128u);
-                // sub-tile h of this CTA: B rows [nb*512 + 256h + 128*rank, +128), the rank's half of MMA h
-                const int32_t n0 = int32_t(nb * Cfg::kBN + pair_rank * 128u);
+                // sub-tile h of this CTA: B rows [nb*BN + HALF_N*h + (HALF_N/2)*rank, +HALF_N/2), the rank's
+                // half of MMA h
+                const int32_t n0 = int32_t(nb * Cfg::kBN + pair_rank * uint32_t(Cfg::kBBoxRows));
                 const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
                 const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb, ++fills) {
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                         const uint64_t b_desc = smem_desc_sw128(b_addr + uint32_t(h) * Cfg::kBSubBytes);
 #pragma unroll
                         for (int kk = 0; kk < kBlockK / 16; ++kk)
-                            ptx::mma_f16<2>(tmem_base + uint32_t(h * Cfg::kHalfN), a_desc + uint64_t(2 * kk),
+                            ptx::mma_f16<2>(tmem_base + uint32_t(h * Cfg::kHalfCol), a_desc + uint64_t(2 * kk),
                                             b_desc + uint64_t(2 * kk), idesc, (kb != k_lo || kk != 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(bar_empty(stage), uint16_t(0x3u));
@@ -205,7 +219,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         const uint32_t half = (warp - 2u) >> 2;     // accumulator columns [256 half, +256)
         const uint32_t buf = base + Cfg::kOffStore + (warp - 2u) * kStoreBufBytes;
         const uint32_t row_addr = buf + lane * 128u;
-        const uint32_t t_col = tmem_base + ((quarter * 32u) << 16) + half * uint32_t(Cfg::kHalfN);
+        const uint32_t t_col = tmem_base + ((quarter * 32u) << 16) + half * uint32_t(Cfg::kHalfCol);
+        constexpr int kHeld = Cfg::kFullChunks - 1;
         uint32_t acc_phase = 0;
         for_each_segment<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
             uint32_t mb, nb;
@@ -217,7 +232,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
             acc_phase ^= 1u;
             ptx::tc_fence_after_sync();
             const bool live = (row0 < p.m) && (col0 < p.n);
-            uint32_t held[3][32];  // columns 64..255 of this warp's piece, as packed fp16 pairs
+            uint32_t held[kHeld][32];             // 64-column chunks 1.. of this warp's piece, packed fp16 pairs
+            uint32_t tail[Cfg::kTail ? 16 : 1];   // the last 32 columns when HALF_N mod 64 = 32
             if (live) {
                 // Columns 0..63 go straight to the staging buffer (its previous store was issued a
                 // whole main loop ago); the rest wait in registers.  32 columns per load keep the
@@ -236,7 +252,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                     stage_row_sw128(row_addr, lane, w);
                 }
 #pragma unroll
-                for (int c = 1; c < 4; ++c) {
+                for (int c = 1; c <= kHeld; ++c) {
 #pragma unroll
                     for (int s = 0; s < 2; ++s) {
                         uint32_t r[32];
@@ -244,6 +260,12 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
 #pragma unroll
                         for (int j = 0; j < 16; ++j) held[c - 1][16 * s + j] = pack_half2(r[2 * j], r[2 * j + 1]);
                     }
+                }
+                if constexpr (Cfg::kTail) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32_wait(t_col + uint32_t(64 * Cfg::kFullChunks), r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) tail[j] = pack_half2(r[2 * j], r[2 * j + 1]);
                 }
             }
             // tensor memory is free for the next tile as soon as every warp has read its piece; the
@@ -260,7 +282,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                     ptx::bulk_commit_group();
                 }
 #pragma unroll
-                for (int c = 1; c < 4; ++c) {
+                for (int c = 1; c <= kHeld; ++c) {
                     const uint32_t col = col0 + uint32_t(64 * c);
                     if (col < p.n) {
                         if (lane == 0) ptx::bulk_wait_group_read<0>();
@@ -270,6 +292,24 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                         __syncwarp();
                         if (lane == 0) {
                             ptx::tma_store_2d(&p.tmap_c, buf, int32_t(col), int32_t(row0));
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                }
+                if constexpr (Cfg::kTail) {
+                    const uint32_t col = col0 + uint32_t(64 * Cfg::kFullChunks);
+                    if (col < p.n) {
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();
+                        __syncwarp();
+                        const uint32_t row32 = buf + lane * 64u;  // unswizzled 64-byte rows, box {32, 32}
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            ptx::st_shared_v4(row32 + (uint32_t(j) << 4), tail[4 * j], tail[4 * j + 1],
+                                              tail[4 * j + 2], tail[4 * j + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&p.tmap_c32, buf, int32_t(col), int32_t(row0));
                             ptx::bulk_commit_group();
                         }
                     }

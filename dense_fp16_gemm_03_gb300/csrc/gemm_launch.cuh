@@ -69,11 +69,11 @@ cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &para
                              KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes, CG * MC);
 }
 
-template <int ST>
+template <int ST, int HN>
 cudaError_t launch_wide(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
 {
-    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST>), plan, params, stream,
-                             kWideThreads, WideCfg<ST>::kSmemBytes, 2);
+    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST, HN>), plan, params, stream,
+                             kWideThreads, WideCfg<ST, HN>::kSmemBytes, 2);
 }
 
 #define GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, EP)                                                        \
@@ -87,12 +87,12 @@ cudaError_t launch_wide(const gemm_f16_plan_t &plan, const KernelParams &params,
 #define GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, CT) GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, 2)
 #define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF) GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, false)
 #define GEMM_VARIANT(CG, BN, ST, MC) GEMM_VARIANT_L(CG, BN, ST, MC, true, true)
-#define GEMM_VARIANT_WIDE(ST)                                                                                  \
+#define GEMM_VARIANT_WIDE(ST, HN)                                                                              \
     Variant                                                                                                    \
     {                                                                                                          \
-        2, WideCfg<ST>::kBN, ST, 1, 0, 0, WideCfg<ST>::kSmemBytes,                                             \
-            reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST>), &launch_wide<ST>, kWideThreads,      \
-            WideCfg<ST>::kBBoxRows                                                                             \
+        2, WideCfg<ST, HN>::kBN, ST, 1, 0, 0, WideCfg<ST, HN>::kSmemBytes,                                     \
+            reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST, HN>), &launch_wide<ST, HN>,            \
+            kWideThreads, WideCfg<ST, HN>::kBBoxRows                                                           \
     }
 
 const Variant kVariants[] = {
@@ -114,10 +114,22 @@ const Variant kVariants[] = {
     // operands swapped (C^T = B . A^T, tiles stored transposed), for few rows of A
     GEMM_VARIANT_X(2, 128, 8, 1, true, true, true),  // 13: B rows on the pair's M = 256, A rows on N = 128
     GEMM_VARIANT_X(1, 128, 6, 1, true, true, true),  // 14: one CTA, 128 B rows x 128 A rows
-    // 256 x 512 tile on a CTA pair, one accumulator filling tensor memory (no stream-K tail)
-    GEMM_VARIANT_WIDE(4),  // 15
+    // wide tiles on a CTA pair, one accumulator filling tensor memory (no stream-K tail)
+    GEMM_VARIANT_WIDE(4, 256),  // 15: 256 x 512
+    GEMM_VARIANT_WIDE(4, 224),  // 16: 256 x 448 (fills the last wave where N / 512 would leave it idle)
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
+
+bool is_wide(const Variant &var)
+{
+    return var.threads == kWideThreads;
+}
+
+// Columns per MMA: a wide tile runs two MMAs side by side.
+int mma_n(const Variant &var)
+{
+    return is_wide(var) ? var.bn / 2 : var.bn;
+}
 
 // ------------------------------------------------------- tensor maps
 
@@ -188,7 +200,7 @@ gemm_status_t encode_tensor_maps(const Variant &var, const gemm_f16_plan_t &plan
         st = encode_matrix(enc, &params->tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, true, 4);
     }
     if (st != GEMM_OK) return st;
-    if (var.bn % 64 != 0 && var.layout == 0) {
+    if (mma_n(var) % 64 != 0 && var.layout == 0) {  // a last 32-column store box per tile (or tile half)
         st = encode_matrix(enc, &params->tmap_c32, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, false);
         if (st != GEMM_OK) return st;
     }

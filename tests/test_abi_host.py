@@ -181,7 +181,10 @@ def test_stream_k_plan_invariants(L, shape, variant):
                 assert workers == slots
             else:                                                     # few tiles: sized against the fix-up
                 assert workers == min(slots, max(1, int(p.num_tiles * math.sqrt(0.18 * p.k_blocks) + 0.5)))
-                assert workers > p.num_tiles
+                # the tail gives each cluster num_tiles / workers tiles: fewer than the most any
+                # cluster would run data-parallel (a second, partial wave counts whole)
+                dp_waves = -(-p.num_tiles // min(p.num_tiles, slots))
+                assert p.num_tiles < dp_waves * workers
         else:                                                         # too little work to split
             assert p.workspace_bytes == 0 and p.dp_tiles == p.num_tiles
         q = G.gemm_f16_nt_plan_for(m, n, k, sms, 0, variant, 0, 0)
@@ -257,10 +260,14 @@ def test_k_rotation_rule(L):
 @pytest.mark.parametrize("shape,variant,stream_k,split", [
     ((8192, 8192, 8192), 15, 0, False),    # 256 x 512 pair tiles: least data per flop, 96% of the waves busy
     ((6144, 6144, 6144), 15, 0, False),
-    ((4096, 8192, 4096), 2, 0, False),     # 256 x 256 pair tiles fill 96% of their waves, the wide ones 84%
-    ((3000, 5000, 4096), 4, 1, False),     # multicast pairs with a stream-K tail beat a 79%-busy wide tile
+    ((4096, 8192, 4096), 16, 0, False),    # 256 x 448 tiles fill exactly 4 waves; 256 x 512 ones 84% of theirs
+    ((3000, 5000, 4096), 4, 1, False),     # with 38 clusters of four, multicast pairs and a stream-K tail
+                                           # (3.3 waves) edge out 144 tiles of 256 x 448 (95% of 2 waves);
+                                           # GB300 fits 36, and there the 256 x 448 tile wins
     ((256, 256, 256), 2, 0, False),        # one tile: the wide tile would compute twice the area
-    ((128, 16384, 16384), 1, 0, False),    # M <= 128: single-CTA 128 x 128 tiles, rotated K walk
+    ((128, 16384, 16384), 13, 0, False),   # M <= 128, B rows for 64 of 76 pairs: swapped pair tiles, rotated
+    ((100, 20000, 8192), 13, 1, False),    # 79 pair tiles for 76 pairs: a stream-K tail, not a second wave
+    ((128, 8192, 8192), 1, 0, True),       # 32 pair tiles would idle most pairs: 128 x 128 tiles, K split
     ((256, 256, 1 << 20), 2, 0, True),     # one tile, long K: split-K over every cluster
     ((512, 512, 65536), 4, 0, True),
     ((200, 1000, 3000), 2, 0, True),       # few tiles: split-K rather than a tail without a whole wave

@@ -21,7 +21,7 @@ def _gpu():
     require_gpu()
 
 
-@pytest.mark.parametrize("variant", [0, 2, 15])
+@pytest.mark.parametrize("variant", [0, 2, 15, 16])
 def test_starved_wait_reports_timeout_and_recovers(variant):
     M, N, K = 256, 512, 640
     A, B = inputs.make_operands(M, N, K, "eighths", seed=77)

@@ -33,7 +33,7 @@ def _variants(stream_k=False):
 
 # ------------------------------------------------------------------ small
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15, 16])
 def test_square_256_exact_every_variant(variant):
     w = inputs.BY_NAME["square_256"]
     A, B = inputs.workload_operands(w)
@@ -47,11 +47,11 @@ def test_day78_lcg_operands_256():
 
 
 RAGGED = [(1, 8, 8), (3, 8, 16), (129, 264, 72), (128, 256, 64), (257, 136, 200), (300, 520, 136),
-          (640, 1032, 520), (1000, 1000, 1000), (96, 2056, 264)]
+          (640, 1032, 520), (1000, 1000, 1000), (96, 2056, 264), (300, 872, 200)]
 
 
 @pytest.mark.parametrize("shape", RAGGED)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15, 16])
 def test_ragged_exact(shape, variant):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "eighths", seed=M + 7 * N + 13 * K)
@@ -89,6 +89,18 @@ def test_stream_k_exact(shape, variant):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "eighths", seed=3 * M + N + K)
     assert_parity(run_gpu(A, B, variant=variant, stream_k=1), A, B, exact=True)
+
+
+@pytest.mark.parametrize("variant", [1, 13])
+def test_stream_k_tail_past_one_wave_exact(variant):
+    """A few more tiles than clusters (one row of them, K in 9 blocks, the last ragged): the automatic
+    tail spreads every tile over all clusters, each taking a little over one tile, so nearly every
+    tile is split in two and finished by the cluster that holds its first K block."""
+    M, N, K = 100, 128 * (num_sms() + 6), 520
+    plan = G.gemm_f16_nt_plan_ex(M, N, K, variant, 0, -1)
+    assert plan.stream_k == 1 and plan.dp_tiles == 0 and plan.num_tiles > plan.grid // plan.cluster
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=N + variant)
+    assert_parity(run_gpu(A, B, variant=variant, stream_k=-1), A, B, exact=True)
 
 
 @pytest.mark.parametrize("shape", [(777, 1000, 1536), (1024, 1024, 4096), (128, 2048, 16384)])
