@@ -91,7 +91,7 @@ struct KernelParams {
     CUtensorMap tmap_a;   // A [M, K]: box {64, 128}
     CUtensorMap tmap_b;   // B [N, K]: box {64, BN / CG}
     CUtensorMap tmap_c;   // C [M, N]: fp16 box {64, 32} (fp32 box {32, 32}), 128-byte swizzle
-    CUtensorMap tmap_c32; // C [M, N]: box {32, 32}, no swizzle (last chunk of a tile N % 64 == 32)
+    CUtensorMap tmap_c32; // C [M, N]: box {32, 32}, 64-byte swizzle (last chunk of a tile N % 64 == 32)
     Raster raster;
     uint32_t m, n, k;
     uint32_t num_tiles;
@@ -610,10 +610,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                                 ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), w0, w1, w2, w3);
                             }
                         } else {
-                            const uint32_t row_addr = buf + lane * 64u;  // unswizzled 64-byte rows
+                            // 64-byte rows, 64-byte swizzle: 16-byte chunk j of row r sits at chunk
+                            // j ^ ((r / 2) mod 4), so each quarter warp's stores hit distinct banks
+                            const uint32_t row_addr = buf + lane * 64u;
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                ptx::st_shared_v4(row_addr + (uint32_t(j) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                                ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ ((lane >> 1) & 3u)) << 4),
+                                                  pack_half2(r[8 * j + 0], r[8 * j + 1]),
                                                   pack_half2(r[8 * j + 2], r[8 * j + 3]),
                                                   pack_half2(r[8 * j + 4], r[8 * j + 5]),
                                                   pack_half2(r[8 * j + 6], r[8 * j + 7]));

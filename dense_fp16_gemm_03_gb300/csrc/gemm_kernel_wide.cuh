@@ -301,11 +301,12 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                     if (col < p.n) {
                         if (lane == 0) ptx::bulk_wait_group_read<0>();
                         __syncwarp();
-                        const uint32_t row32 = buf + lane * 64u;  // unswizzled 64-byte rows, box {32, 32}
+                        // box {32, 32}: 64-byte rows, 64-byte swizzle (chunk j of row r at j ^ ((r / 2) mod 4))
+                        const uint32_t row32 = buf + lane * 64u;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            ptx::st_shared_v4(row32 + (uint32_t(j) << 4), tail[4 * j], tail[4 * j + 1],
-                                              tail[4 * j + 2], tail[4 * j + 3]);
+                            ptx::st_shared_v4(row32 + ((uint32_t(j) ^ ((lane >> 1) & 3u)) << 4), tail[4 * j],
+                                              tail[4 * j + 1], tail[4 * j + 2], tail[4 * j + 3]);
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {

@@ -153,11 +153,11 @@ gemm_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
 }
 
 // Row-major fp16 (or, with elem_bytes 4, fp32) matrix of `rows` x `cols`
-// (cols contiguous), boxes of box_cols x box_rows (128-byte swizzled unless
-// `swizzle` is false), zero fill outside the matrix.
+// (cols contiguous), boxes of box_cols x box_rows in shared memory laid out
+// with `swizzle`, zero fill outside the matrix.
 gemm_status_t encode_matrix(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *map, const void *ptr,
-                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows, bool swizzle = true,
-                            uint32_t elem_bytes = 2)
+                            uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                            CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, uint32_t elem_bytes = 2)
 {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * elem_bytes};
@@ -165,7 +165,7 @@ gemm_status_t encode_matrix(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
 }
@@ -190,18 +190,21 @@ gemm_status_t encode_tensor_maps(const Variant &var, const gemm_f16_plan_t &plan
         st = encode_matrix(enc, &params->tmap_b, kb, uint64_t(kn), uint64_t(plan.k), kBlockK, uint32_t(var.b_box));
         if (st != GEMM_OK) return st;
         if (var.swap)  // C [m, n] written in transposed tiles: boxes of 32 columns x 64 rows, unswizzled
-            st = encode_matrix(enc, &params->tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, 64, false);
+            st = encode_matrix(enc, &params->tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, 64,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
         else
             st = encode_matrix(enc, &params->tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), kStoreCols, kStoreRows);
     } else {
         // B [K, N]: 64-column boxes of 64 K rows; D [M, N] fp32: 32-column boxes
         st = encode_matrix(enc, &params->tmap_b, b, uint64_t(plan.k), uint64_t(plan.n), 64, kBlockK);
         if (st != GEMM_OK) return st;
-        st = encode_matrix(enc, &params->tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, true, 4);
+        st = encode_matrix(enc, &params->tmap_c, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows,
+                           CU_TENSOR_MAP_SWIZZLE_128B, 4);
     }
     if (st != GEMM_OK) return st;
     if (mma_n(var) % 64 != 0 && var.layout == 0) {  // a last 32-column store box per tile (or tile half)
-        st = encode_matrix(enc, &params->tmap_c32, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows, false);
+        st = encode_matrix(enc, &params->tmap_c32, c, uint64_t(plan.m), uint64_t(plan.n), 32, kStoreRows,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != GEMM_OK) return st;
     }
     return GEMM_OK;

@@ -138,9 +138,9 @@ def test_stream_k_plan_shape():
 
 
 def test_workspace_entry_point_rejects_small_workspace():
-    M, N, K = 3000, 5000, 4096
+    M, N, K = 1000, 1000, 1000
     need = G.gemm_f16_nt_workspace_size(M, N, K)
-    assert need > 0                               # the automatic plan has a stream-K tail here
+    assert need > 0                               # the automatic plan splits K here (few tiles)
     a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     b = torch.zeros((N, K), dtype=torch.float16, device="cuda")
     c = torch.zeros((M, N), dtype=torch.float16, device="cuda")

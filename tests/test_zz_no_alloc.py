@@ -3,8 +3,9 @@
 It exists for callers that may not allocate device memory (code inside a
 host that owns every allocation through its own pool, paths that must not
 call cudaMalloc/cudaFree because those can synchronize the device).  It runs
-the stream-K GEMM with its scratch taken from an array built into the
-library, so its results must agree with the workspace entry point
+plans that need scratch (a stream-K tail, split K) with that scratch taken
+from an array built into the library, so its results must agree with the
+workspace entry point
 (gemm_f16_nt_ws with a caller-allocated workspace) within the parity bound
 the other tests use, on consecutive calls that reuse that one array.
 
@@ -29,12 +30,14 @@ def _within_bound(got_bits, ref_bits, A, B):
     assert rep.ok, repr(rep)
 
 
-@pytest.mark.parametrize("shape,dist", [((3000, 5000, 4096), "eighths"), ((1024, 2048, 4096), "normal")])
+# 100 x 20000 x 2048: one strip of B rows a little past one wave of tiles, a stream-K tail;
+# 1024 x 2048 x 4096: few tiles, split K
+@pytest.mark.parametrize("shape,dist", [((100, 20000, 2048), "eighths"), ((1024, 2048, 4096), "normal")])
 def test_noalloc_matches_workspace_entry_point_twice(shape, dist):
     require_gpu()
     M, N, K = shape
     need = G.gemm_f16_nt_workspace_size(M, N, K)
-    assert 0 < need <= G.STATIC_SCRATCH_BYTES     # a stream-K plan: the scratch path runs
+    assert 0 < need <= G.STATIC_SCRATCH_BYTES     # a plan with scratch: the built-in array serves it
     A, B = inputs.make_operands(M, N, K, dist, seed=M + N)
     a, b = to_dev(A), to_dev(B)
 
