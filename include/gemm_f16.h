@@ -76,8 +76,8 @@ typedef struct gemm_f16_plan {
     int32_t cta_group;       /* 1: one CTA per MMA tile; 2: a CTA pair (cluster of 2) shares one */
     int32_t block_m;         /* output rows per cluster tile (128 * cta_group, times the CTA pairs a
                                 multicast cluster stacks along M) */
-    int32_t block_n;         /* output columns per cluster tile (the 256 x 512 tile: 512, two MMAs of N = 256;
-                                single CTAs sharing A by multicast: N times the CTAs along N) */
+    int32_t block_n;         /* output columns per cluster tile (wide tiles: 512 or 448, two MMAs of N = 256
+                                or 224; single CTAs sharing A by multicast: N times the CTAs along N) */
     int32_t block_k;         /* K depth of one pipeline stage (64) */
     int32_t stages;          /* shared-memory ring depth */
     int32_t raster_width;    /* N-columns per raster group (>= 1) */
@@ -112,9 +112,9 @@ typedef struct gemm_f16_plan {
  * shared by launches that overlap on the GPU.  Every cluster of the grid
  * must be resident at once; the plan's
  * grid never exceeds that.  The fp32 partial sums change the rounding order
- * of split tiles only within the fp32 accumulation error.  The 256 x 512
- * tile (block_n 512) has no stream-K tail: asking for one is
- * GEMM_ERR_INVALID_ARG, and automatic plans never give it one.
+ * of split tiles only within the fp32 accumulation error.  The wide tiles
+ * (256 x 512 and 256 x 448, block_n > 256) have no stream-K tail: asking for
+ * one is GEMM_ERR_INVALID_ARG, and automatic plans never give them one.
  *
  * Split-K ("split_k == S > 1", stream_k 0): for products with fewer tiles
  * than resident clusters and a long K.  Each tile's K blocks are cut into S
@@ -133,7 +133,8 @@ typedef struct gemm_f16_plan {
 const char *gemm_f16_status_string(gemm_status_t status);
 
 /* Number of compiled kernel variants, and the shape of one of them: CTAs
- * per MMA (cta_group), MMA tile N, ring depth, dynamic shared memory, CTAs
+ * per MMA (cta_group), tile N of one CTA or pair (a wide tile's two MMAs
+ * together), ring depth, dynamic shared memory, CTAs
  * per cluster, layout (as in gemm_f16_plan_t) and whether it computes the
  * transposed product C^T = B . A^T with the operands swapped (for products
  * with few rows of A; a plan of such a variant has tiles_m over n and
