@@ -208,7 +208,8 @@ def _segments(p):
     return out
 
 
-@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (128, 256, 8192)])
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (128, 256, 8192),
+                                   (100, 20000, 8192), (128, 24576, 8192)])
 def test_stream_k_covers_every_k_block_once(L, shape):
     m, n, k = shape
     for variant in range(G.gemm_f16_variant_count()):
