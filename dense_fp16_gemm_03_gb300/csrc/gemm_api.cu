@@ -371,7 +371,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.dp_tiles = p.num_tiles;
     p.sk_iters = 0;
     p.workspace_bytes = 0;
-    // the wide variant has no stream-K tail: asking for one is an error, the automatic choice skips it
+    // the wide variants have no stream-K tail: asking for one is an error, the automatic choice skips it
     const bool sk_capable = !is_wide(var);
     if (stream_k == 1 && !sk_capable) return GEMM_ERR_INVALID_ARG;
     // rotation or a stream-K tail (tail_choice); with the tail forbidden or unavailable, rotation alone
