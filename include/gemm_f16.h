@@ -175,21 +175,21 @@ gemm_status_t gemm_f16_nt_plan_ex(int64_t m, int64_t n, int64_t k, int32_t varia
                                   int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out);
 
 /* Device workspace (bytes) gemm_f16_nt_ws needs for this shape on the
- * current device (the stream-K partial tiles and flags); 0 when the chosen
- * plan needs none. */
+ * current device (the stream-K partial tiles and flags, or the split-K
+ * parts); 0 when the chosen plan needs none. */
 gemm_status_t gemm_f16_nt_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes);
 
 /*
  * C = A . B^T on `stream`.  a: device pointer to M*K fp16, b: device pointer
  * to N*K fp16, c: device pointer to M*N fp16.  Plans automatically among the
- * plans that need no workspace (no stream-K tail).
+ * plans that need no workspace (no stream-K tail, no split K).
  */
 gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
                           void *c, gemm_stream_t stream);
 
 /* As gemm_f16_nt with a caller-owned device workspace of ws_bytes bytes,
- * 256-byte aligned: uses the automatic plan, with a stream-K tail when it
- * pays.  workspace may be NULL/0 when gemm_f16_nt_workspace_size reports 0;
+ * 256-byte aligned: uses the automatic plan, with a stream-K tail or split K
+ * when it pays.  workspace may be NULL/0 when gemm_f16_nt_workspace_size reports 0;
  * too small -> GEMM_ERR_WORKSPACE, misaligned -> GEMM_ERR_ALIGNMENT.  Calls
  * that share one workspace must not overlap on the GPU. */
 gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
