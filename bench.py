@@ -318,7 +318,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--variant", type=int, default=-1, help="force a compiled kernel variant (measurement)")
     ap.add_argument("--raster", type=int, default=0, help="force a raster width (measurement)")
-    ap.add_argument("--stream-k", type=int, default=-1, help="force stream-K off (0) or on (1) (measurement)")
+    ap.add_argument("--stream-k", type=int, default=-1,
+                    help="force no split (0), a stream-K tail (1) or split-K (2) (measurement)")
     ap.add_argument("--ablation", action="store_true",
                     help="time the pipeline ablation ladder (one JSON line per rung) instead of the bench step")
     ap.add_argument("--rounds", type=int, default=3, help="interleaved rounds of the ablation ladder")
