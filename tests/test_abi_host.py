@@ -191,6 +191,30 @@ def test_stream_k_plan_invariants(L, shape, variant):
         assert q.stream_k == 0 and q.workspace_bytes == 0 and q.dp_tiles == q.num_tiles
 
 
+@pytest.mark.parametrize("tiles_over_slots,expect_tail", [
+    (5, True),        # a few tiles past one wave: each cluster takes a little over one tile
+    (152, False),     # exactly two waves: whole tiles already balance
+    (0, False),       # exactly one wave
+    (100, True),      # a second wave two-thirds full
+])
+def test_forced_tail_only_when_it_shortens_the_longest_cluster(L, tiles_over_slots, expect_tail):
+    """Variant 1 (128 x 128 tiles, 152 slots on 152 SMs) over one strip of B rows: a forced stream-K
+    tail is kept exactly when it gives some cluster less work than the data-parallel waves would."""
+    tiles = 152 + tiles_over_slots
+    p = G.gemm_f16_nt_plan_for(128, 128 * tiles, 4096, 152, 0, 1, 0, 1)
+    assert p.num_tiles == tiles
+    slots = 152
+    full_waves = tiles // slots
+    dp = (full_waves - 1) * slots if full_waves >= 1 else 0
+    left = tiles - dp
+    assert bool(p.stream_k) == expect_tail
+    if p.stream_k:
+        workers = p.grid // p.cluster
+        assert p.dp_tiles == dp and left < -(-left // min(left, slots)) * workers
+    else:
+        assert p.dp_tiles == tiles and p.workspace_bytes == 0
+
+
 def _segments(p):
     """The kernel's segment walk for every cluster, written out independently."""
     workers = p.grid // p.cluster
