@@ -293,7 +293,8 @@ int64_t splitk_workspace_bytes(int64_t tiles, int64_t parts, int32_t cluster, in
     return round_up(tiles * parts * cluster * 128 * int64_t(block_n) * 4, 256);
 }
 
-// Split-K needs the fp16 [N,K] layout without operand swap and tiles of whole 64-column chunks.
+// Split-K needs the fp16 [N,K] layout without operand swap and tiles of whole 64-column chunks up to
+// 256 columns (not the wide tiles).
 bool split_capable(const Variant &var)
 {
     return var.layout == 0 && !var.swap && var.bn % 64 == 0 && var.bn <= 256;

@@ -125,8 +125,8 @@ typedef struct gemm_f16_plan {
  * fp16 result.  Workspace: tiles x S x (CTAs per cluster) parts of
  * 128 x block_n fp32.  Unlike the stream-K tail, no one cluster adds many
  * parts, so a tile's K can be spread over the whole GPU.  Variants with
- * fp16 C, B [N,K], tiles of whole 64-column chunks and no operand swap only
- * (0-4, 11, 12).
+ * fp16 C, B [N,K], tiles of whole 64-column chunks up to 256 columns and no
+ * operand swap only (0-4, 11, 12).
  */
 
 /* Human-readable name of a status code (static string, never NULL). */
