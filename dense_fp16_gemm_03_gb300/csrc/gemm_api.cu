@@ -586,6 +586,16 @@ gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_
     return make_plan(m, n, k, num_sms, max_clusters, variant, raster_width, stream_k, out);
 }
 
+gemm_status_t gemm_f16_nt_plan_for_clusters(int64_t m, int64_t n, int64_t k, int32_t num_sms,
+                                            const int32_t *clusters_by_variant, int32_t count, int32_t variant,
+                                            int32_t raster_width, int32_t stream_k, gemm_f16_plan_t *out)
+{
+    if (!clusters_by_variant || count != kNumVariants) return GEMM_ERR_INVALID_ARG;
+    for (int v = 0; v < kNumVariants; ++v)
+        if (clusters_by_variant[v] < 1) return GEMM_ERR_INVALID_ARG;
+    return make_plan(m, n, k, num_sms, 0, variant, raster_width, stream_k, out, clusters_by_variant);
+}
+
 }  // extern "C"
 
 namespace {

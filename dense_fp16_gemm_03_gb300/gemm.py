@@ -73,7 +73,8 @@ class Plan(ctypes.Structure):
 # every symbol the public header declares
 EXPORTED = [
     "gemm_f16_status_string", "gemm_f16_variant_count", "gemm_f16_variant_info",
-    "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_plan_ex", "gemm_f16_nt_workspace_size",
+    "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_plan_for_clusters", "gemm_f16_nt_plan_ex",
+    "gemm_f16_nt_workspace_size",
     "gemm_f16_nt", "gemm_f16_nt_ws", "gemm_f16_nt_run", "gemm_f16_nt_host",
     "gemm_f16_take_device_error", "gemm_f16_raster_coord", "gemm_f16_fast_divmod",
     "gemm_f16_nt_run_stall_test", "gemm_f16_nt_noalloc",
@@ -100,6 +101,7 @@ def lib():
         "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32, pi32]),
         "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),
         "gemm_f16_nt_plan_for": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, P]),
+        "gemm_f16_nt_plan_for_clusters": (ctypes.c_int, [i64, i64, i64, i32, pi32, i32, i32, i32, i32, P]),
         "gemm_f16_nt_plan_ex": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, P]),
         "gemm_f16_nt_workspace_size": (ctypes.c_int, [i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]),
         "gemm_f16_nt": (ctypes.c_int, [i64, i64, i64, vp, vp, vp, vp]),
@@ -175,6 +177,16 @@ def gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters=0, variant=-1, raster_wi
     p = Plan()
     _check(lib().gemm_f16_nt_plan_for(m, n, k, num_sms, max_clusters, variant, raster_width, stream_k,
                                       ctypes.byref(p)), "gemm_f16_nt_plan_for")
+    return p
+
+
+def gemm_f16_nt_plan_for_clusters(m, n, k, num_sms, clusters_by_variant, variant=-1, raster_width=0, stream_k=-1):
+    """Host-only plan with the co-resident cluster count of every variant given (one entry per variant)."""
+    table = (ctypes.c_int32 * len(clusters_by_variant))(*clusters_by_variant)
+    p = Plan()
+    _check(lib().gemm_f16_nt_plan_for_clusters(m, n, k, num_sms, table, len(clusters_by_variant), variant,
+                                               raster_width, stream_k, ctypes.byref(p)),
+           "gemm_f16_nt_plan_for_clusters")
     return p
 
 

@@ -167,6 +167,22 @@ gemm_status_t gemm_f16_nt_plan_for(int64_t m, int64_t n, int64_t k, int32_t num_
                                    int32_t stream_k, gemm_f16_plan_t *out);
 
 /*
+ * As gemm_f16_nt_plan_for, with the co-resident cluster count of every
+ * variant given, as the device entry points measure them
+ * (cudaOccupancyMaxActiveClusters; a 152-SM GB300 fits 76 clusters of two
+ * CTAs and 36 of four): clusters_by_variant[v] for every v below
+ * gemm_f16_variant_count(), which `count` must equal; every entry >= 1
+ * (for single-CTA variants, the SM count).  The automatic variant choice
+ * weighs each candidate with its own count, so this reproduces a device's
+ * plans on the host.  GEMM_ERR_INVALID_ARG for a NULL table, a wrong count
+ * or an entry < 1.  Pure host code.
+ */
+gemm_status_t gemm_f16_nt_plan_for_clusters(int64_t m, int64_t n, int64_t k, int32_t num_sms,
+                                            const int32_t *clusters_by_variant, int32_t count,
+                                            int32_t variant, int32_t raster_width, int32_t stream_k,
+                                            gemm_f16_plan_t *out);
+
+/*
  * As gemm_f16_nt_plan, with the choices of gemm_f16_nt_plan_for overridable
  * (variant / raster_width / stream_k; negative or zero = automatic as
  * there), using the current device's SM count and co-resident cluster count.

@@ -13,6 +13,7 @@ import pytest
 
 from dense_fp16_gemm_03_gb300 import build as pkg_build
 from dense_fp16_gemm_03_gb300 import gemm as G
+from dense_fp16_gemm_03_gb300 import inputs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -213,6 +214,58 @@ def test_forced_tail_only_when_it_shortens_the_longest_cluster(L, tiles_over_slo
         assert p.dp_tiles == dp and left < -(-left // min(left, slots)) * workers
     else:
         assert p.dp_tiles == tiles and p.workspace_bytes == 0
+
+
+def _gb300_clusters():
+    """Co-resident clusters per variant on a 152-SM GB300 (measured: 76 clusters of two CTAs, 36 of
+    four; single CTAs one per SM)."""
+    return [{1: 152, 2: 76, 4: 36}[G.gemm_f16_variant_info(v)["cluster"]] for v in range(G.gemm_f16_variant_count())]
+
+
+def test_gb300_plans_of_the_configured_workloads(L):
+    """The host planner with GB300's cluster counts gives the plans the device runs (seen in the bench
+    lines), and the committed DRAM-traffic captures were taken on exactly those plans."""
+    import json
+    expect = {
+        "square_256": (2, 0, 0, 0),
+        "square_4096": (15, 0, 0, 0),
+        "square_8192": (15, 0, 0, 0),
+        "ragged_3000x5000x4096": (16, 0, 0, 0),
+        "skinny_128x16384x16384": (13, 0, 0, 1),
+    }
+    rec = json.load(open(os.path.join(os.path.dirname(__file__), "..", "profiles", "dram_traffic.json")))
+    for name, (variant, stream_k, split_k, k_rotate) in expect.items():
+        w = inputs.BY_NAME[name]
+        p = G.gemm_f16_nt_plan_for_clusters(w.M, w.N, w.K, 152, _gb300_clusters())
+        assert (p.variant, p.stream_k, p.split_k, p.k_rotate) == (variant, stream_k, split_k, k_rotate), name
+        captured = rec["workloads"].get(name)
+        if captured is not None:
+            assert all(getattr(p, k) == v for k, v in captured["plan"].items()), name
+
+
+def test_cluster_counts_steer_the_tile_choice(L):
+    """3000 x 5000 x 4096: with 38 clusters of four (152 / 4) two multicast pairs with a stream-K tail
+    are estimated cheapest; with GB300's 36 the 256 x 448 tile is."""
+    clusters = _gb300_clusters()
+    assert G.gemm_f16_nt_plan_for_clusters(3000, 5000, 4096, 152, clusters).variant == 16
+    ideal = [152 // G.gemm_f16_variant_info(v)["cluster"] for v in range(G.gemm_f16_variant_count())]
+    p = G.gemm_f16_nt_plan_for_clusters(3000, 5000, 4096, 152, ideal)
+    assert (p.variant, p.stream_k) == (4, 1)
+    assert p.as_dict() == G.gemm_f16_nt_plan_for(3000, 5000, 4096, 152).as_dict()
+
+
+def test_plan_for_clusters_argument_errors(L):
+    n_var = G.gemm_f16_variant_count()
+    p = G.Plan()
+    good = (ctypes.c_int32 * n_var)(*_gb300_clusters())
+    assert L.gemm_f16_nt_plan_for_clusters(256, 256, 256, 152, None, n_var, -1, 0, -1, ctypes.byref(p)) == \
+        G.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_nt_plan_for_clusters(256, 256, 256, 152, good, n_var - 1, -1, 0, -1, ctypes.byref(p)) == \
+        G.GEMM_ERR_INVALID_ARG
+    bad = (ctypes.c_int32 * n_var)(*([0] + _gb300_clusters()[1:]))
+    assert L.gemm_f16_nt_plan_for_clusters(256, 256, 256, 152, bad, n_var, -1, 0, -1, ctypes.byref(p)) == \
+        G.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_nt_plan_for_clusters(256, 256, 256, 152, good, n_var, -1, 0, -1, ctypes.byref(p)) == G.GEMM_OK
 
 
 def _segments(p):
