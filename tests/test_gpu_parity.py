@@ -293,6 +293,19 @@ def test_plan_matches_device():
         assert p.workspace_bytes >= p.grid * (p.block_m // p.cta_group) * p.block_n * 4
 
 
+def test_host_planner_reproduces_device_plans():
+    """On a 152-SM GB300 the device measures 76 co-resident clusters of two CTAs and 36 of four; the
+    host planner given those counts must produce the device's own automatic plans."""
+    if num_sms() != 152:
+        pytest.skip("the cluster table below is GB300's")
+    clusters = [{1: 152, 2: 76, 4: 36}[G.gemm_f16_variant_info(v)["cluster"]]
+                for v in range(G.gemm_f16_variant_count())]
+    for w in inputs.WORKLOADS:
+        dev = G.gemm_f16_nt_plan(w.M, w.N, w.K).as_dict()
+        host = G.gemm_f16_nt_plan_for_clusters(w.M, w.N, w.K, 152, clusters).as_dict()
+        assert dev == host, w.name
+
+
 # ------------------------------------------------------- full workloads
 
 def _full(name):
