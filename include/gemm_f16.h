@@ -17,7 +17,8 @@
  * Ownership: the caller owns every buffer (a, b, c, workspace) and the
  * stream.  The library never allocates or frees device memory and keeps no
  * per-call state; its only device-resident state is one 32-bit error word
- * per device (see gemm_f16_take_device_error).  Launches are asynchronous
+ * per device (see gemm_f16_take_device_error) and the module-static scratch
+ * array of gemm_f16_nt_noalloc.  Launches are asynchronous
  * on `stream`; a, b are only read; c is fully overwritten (no beta, no
  * accumulate).  Overlap of c with a or b is undefined.
  *
@@ -221,7 +222,7 @@ gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const 
  * End-to-end form for host-resident data: copies a_host (M*K fp16) and
  * b_host (N*K fp16) into the caller's device buffers a_dev / b_dev, runs
  * the GEMM into c_dev (automatic plan; the workspace, which may be NULL/0,
- * serves a stream-K tail when it is large enough), and copies c_dev back to
+ * serves a stream-K tail or split K when it is large enough), and copies c_dev back to
  * c_host (M*N fp16).  Asynchronous on `stream`: the work starts after what
  * is already enqueued there and the stream continues after the last copy
  * back; pinned host memory makes the copies truly asynchronous.
