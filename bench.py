@@ -11,9 +11,15 @@ and C resident in HBM.  Prints one JSON line (rank 0).
 on this machine's host cores over a bounded sample of the same workload:
 the only reference that exists for this product is that definition.
 
-Multi-GPU (torchrun, one rank per GPU): each rank runs its own replica of
-the workload (the product needs no exchange); value = all ranks' flops /
-the slowest rank's time ("scaling": "weak").
+After the headline step the line also carries a "workloads" object: every
+configured product (256^3, 4096^3, 8192^3, 3000 x 5000 x 4096 and
+128 x 16384 x 16384) timed back to back through the same entry point, each
+rotating over enough copies of its operands that the launches do not find
+them in L2.
+
+One GPU per process: the library is meant for single-GPU processes (its
+multicast TMA loads read only this GPU's own buffers), so this script
+refuses to run as several ranks (WORLD_SIZE > 1) or with --gpus > 1.
 """
 import argparse
 import hashlib
@@ -35,7 +41,9 @@ from dense_fp16_gemm_03_gb300 import inputs  # noqa: E402
 METRIC = "GEMM TFLOP/s (2MNK/time) at 1 GB300; fraction of dense fp16 tensor peak"
 UNIT = "TFLOP/s"
 NOMINAL_PEAK_TFLOPS = 2250.0      # dense fp16/bf16 tensor peak quoted for GB300
-FALLBACK_PEAK_TFLOPS = 1700.0     # bf16 sustained, measured earlier on a GB300
+FALLBACK_BURST_TFLOPS = 1900.0    # bf16 burst, measured earlier on a GB300 (used without MEASURED_PEAKS.json)
+FALLBACK_SUSTAINED_TFLOPS = 1700.0  # bf16 sustained, same
+FALLBACK_HBM_GBS = 6800.0         # copy bandwidth, same
 L2_BYTES = 129 * 10 ** 6
 KERNEL_SOURCES = ["dense_fp16_gemm_03_gb300/csrc/gemm_kernel.cuh", "dense_fp16_gemm_03_gb300/csrc/gemm_kernel_wide.cuh",
                   "dense_fp16_gemm_03_gb300/csrc/ptx.cuh", "dense_fp16_gemm_03_gb300/csrc/sched.cuh",
@@ -84,6 +92,7 @@ class ClockSampler:
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu_index = gpu_index
@@ -113,17 +122,15 @@ class ClockSampler:
     def mark_end(self):
         self.t1 = time.time()
 
-    def stop(self):
+    def summary(self):
+        """Clocks over the marked region (the samples 50 ms before to 150 ms
+        after it; all samples so far if none fell inside)."""
         if self.proc is None:
             return None
         time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        inside = [s for (t, s) in self.samples if self.t0 is not None and self.t0 - 0.05 <= t <= self.t1 + 0.15]
-        use = inside if inside else [s for (_, s) in self.samples]
+        samples = list(self.samples)
+        inside = [s for (t, s) in samples if self.t0 is not None and self.t0 - 0.05 <= t <= self.t1 + 0.15]
+        use = inside if inside else [s for (_, s) in samples]
         if not use:
             return None
 
@@ -136,8 +143,8 @@ class ClockSampler:
         sm = [num(s[2]) for s in use if len(s) > 2 and num(s[2]) is not None]
         smax = [num(s[3]) for s in use if len(s) > 3 and num(s[3]) is not None]
         power = [num(s[4]) for s in use if len(s) > 4 and num(s[4]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in use for i in range(4) if len(s) > 6 + i and s[6 + i].lower() == "active"})
+        reasons = sorted({self.REASONS[i] for s in use for i in range(4)
+                          if len(s) > 6 + i and s[6 + i].lower() == "active"})
         return {
             "sm_mhz": statistics.median(sm) if sm else None,
             "sm_max_mhz": max(smax) if smax else None,
@@ -146,6 +153,15 @@ class ClockSampler:
             "samples": len(use),
             "samples_in_timed_region": len(inside),
         }
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
 
 
 def cpu_oracle_rate(A, B, target_s=10.0):
@@ -173,19 +189,9 @@ def cpu_oracle_rate(A, B, target_s=10.0):
     return 2.0 * rows * N * K / dt / 1e12, dt, rows
 
 
-def aggregate_throughput(local_ms, flops_per_step, steps, dist=None, device="cpu"):
-    """Whole-job throughput of `steps` replicated steps per rank: the slowest
-    rank's time (max over ranks) bounds the job; every rank did its own
-    steps.  Returns (TFLOP/s, max_ms).  dist: torch.distributed or None."""
-    import torch
-    world = 1
-    max_ms = float(local_ms)
-    if dist is not None and dist.is_initialized():
-        world = dist.get_world_size()
-        t = torch.tensor([max_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
-    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12, max_ms
+def throughput(total_ms, flops_per_step, steps):
+    """TFLOP/s of `steps` steps of `flops_per_step` timed as `total_ms` in all."""
+    return flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
 def dist_setup():
@@ -193,6 +199,45 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def timing_regime(total_ms, clocks):
+    """"sustained" when the timed region ran long enough for the board power
+    cap to matter (a second or more of back-to-back launches, or sw_power_cap
+    seen by the clock sampler inside it), else "burst"."""
+    if total_ms >= 1000.0:
+        return "sustained"
+    if clocks and "sw_power_cap" in (clocks.get("reasons") or []):
+        return "sustained"
+    return "burst"
+
+
+def tensor_roofline(achieved, regime, peaks):
+    """Roofline of a contraction: the measured cuBLAS bf16 rate of the same
+    regime (burst for a short timed region, sustained for one under the
+    power cap) is the denominator; fp16 and bf16 share the nominal tensor
+    rate.  Both fractions are reported."""
+    burst = sustained = None
+    if peaks:
+        burst = float(peaks.get("bf16_tflops") or 0.0) or None
+        sustained = float(peaks.get("bf16_tflops_sustained") or 0.0) or None
+    if regime == "sustained" and sustained:
+        peak, note = sustained, "of measured: cuBLAS bf16 sustained (timed region under the power cap); fp16 rate = bf16 rate"
+    elif burst:
+        peak, note = burst, "of measured: cuBLAS bf16 burst (short timed region); fp16 rate = bf16 rate"
+    elif sustained:
+        peak, note = sustained, "of measured: cuBLAS bf16 sustained (no burst figure); fp16 rate = bf16 rate"
+    elif regime == "sustained":
+        peak, note = FALLBACK_SUSTAINED_TFLOPS, "of fallback (bf16 sustained)"
+    else:
+        peak, note = FALLBACK_BURST_TFLOPS, "of fallback (bf16 burst)"
+    return {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+        "regime": regime, "peak_source": note,
+        "burst_peak": burst, "frac_burst": (achieved / burst) if burst else None,
+        "sustained_peak": sustained, "frac_sustained": (achieved / sustained) if sustained else None,
+        "frac_of_nominal_2250": achieved / NOMINAL_PEAK_TFLOPS,
+    }
 
 
 def run_reference(args, w, world, rank):
@@ -278,8 +323,6 @@ def run_ablation(args, w):
     st, code = G.gemm_f16_take_device_error()
     if st != G.GEMM_OK:
         raise RuntimeError("kernel reported error word 0x%x" % code)
-    sampler.mark_begin()
-    sampler.mark_end()
     sampler.stop()
     for i, (label, page, variant, raster, one_tile, plan) in enumerate(rungs):
         ms = statistics.median(times[i])
@@ -307,6 +350,76 @@ def workload_config(w):
     }
 
 
+def to_device(x, dev):
+    import torch
+    return torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev)
+
+
+def time_workload(G, w, dev, stream, sampler, launches, warmup, peaks):
+    """Time `launches` back-to-back launches of the automatic plan of workload
+    `w` through gemm_f16_nt_ws, rotating over enough copies of A, B and C that
+    their bytes exceed twice the L2 (so no launch finds its operands there).
+    One CUDA event pair on the launching stream brackets the launches."""
+    import torch
+    A, B = inputs.workload_operands(w)
+    a0, b0 = to_device(A, dev), to_device(B, dev)
+    sets = max(1, min(1024, -(-2 * L2_BYTES // w.algorithmic_bytes)))
+    bufs = [(a0, b0, torch.empty((w.M, w.N), dtype=torch.float16, device=dev))]
+    for _ in range(sets - 1):
+        bufs.append((a0.clone(), b0.clone(), torch.empty((w.M, w.N), dtype=torch.float16, device=dev)))
+    plan = G.gemm_f16_nt_plan(w.M, w.N, w.K)
+    ws = G.workspace_for(plan, dev)
+    for i in range(warmup):
+        a, b, c = bufs[i % sets]
+        G.gemm_f16_nt_ws(a, b, c, ws, stream=stream)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    e0.record(stream)
+    h0 = time.perf_counter()
+    for i in range(launches):
+        a, b, c = bufs[i % sets]
+        G.gemm_f16_nt_ws(a, b, c, ws, stream=stream)
+    host_s = time.perf_counter() - h0
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    st, code = G.gemm_f16_take_device_error(stream)
+    if st != G.GEMM_OK:
+        raise RuntimeError("%s: kernel reported error word 0x%x" % (w.name, code))
+    ms = e0.elapsed_time(e1) / launches
+    mhz = [float(s[2]) for (t, s) in list(sampler.samples) if len(s) > 2 and t0 - 0.05 <= t <= t1 + 0.15
+           and s[2].replace(".", "", 1).isdigit()]
+    reasons = sorted({n for (t, s) in list(sampler.samples) if t0 - 0.05 <= t <= t1 + 0.15
+                      for i, n in enumerate(ClockSampler.REASONS) if len(s) > 6 + i and s[6 + i].lower() == "active"})
+    regime = timing_regime(ms * launches, {"reasons": reasons})
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    entry = {
+        "M": w.M, "N": w.N, "K": w.K, "distribution": w.dist, "seed": w.seed,
+        "ms": ms, "tflops": tflops, "launches": launches, "operand_copies": sets,
+        "host_us_per_call": host_s / launches * 1e6,
+        "sm_mhz": statistics.median(mhz) if mhz else None, "clock_reasons": reasons,
+        "plan": {k: getattr(plan, k) for k in ("variant", "block_m", "block_n", "grid", "stream_k", "split_k",
+                                               "k_rotate", "raster_width")},
+        "roofline": tensor_roofline(tflops, regime, peaks),
+        "algorithmic_bytes": w.algorithmic_bytes,
+        "algorithmic_gbs": w.algorithmic_bytes / (ms * 1e-3) / 1e9,
+    }
+    hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
+    if w.flops / w.algorithmic_bytes < (entry["roofline"]["peak"] * 1e12) / (hbm * 1e9):
+        # below the ridge point: HBM bounds the product
+        entry["roofline"] = {
+            "bound": "hbm", "achieved": entry["algorithmic_gbs"], "peak": hbm, "unit": "GB/s",
+            "frac": entry["algorithmic_gbs"] / hbm, "regime": regime,
+            "peak_source": "of measured: copy bandwidth" if peaks and peaks.get("hbm_gbs") else "of fallback",
+            "tensor": entry["roofline"],
+        }
+    del bufs
+    torch.cuda.empty_cache()
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -316,6 +429,9 @@ def main():
     ap.add_argument("--workload", default="square_8192", choices=sorted(inputs.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip timing the other configured products")
+    ap.add_argument("--workload-launches", type=int, default=400,
+                    help="launches per configured product in the workloads object")
     ap.add_argument("--variant", type=int, default=-1, help="force a compiled kernel variant (measurement)")
     ap.add_argument("--raster", type=int, default=0, help="force a raster width (measurement)")
     ap.add_argument("--stream-k", type=int, default=-1,
@@ -330,31 +446,29 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
+    if world > 1 or args.gpus != 1:
+        print("bench.py: this library is for single-GPU processes (it has no multi-GPU path); "
+              "run one process on one GPU (WORLD_SIZE=%d, --gpus %d)" % (world, args.gpus), file=sys.stderr)
+        return 2
     if args.ablation:
         return run_ablation(args, w)
 
     import torch
     from dense_fp16_gemm_03_gb300 import gemm as G
 
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(0)
     G.lib()
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
     A, B = inputs.workload_operands(w)
-    a = torch.from_numpy(A.view(np.int16)).view(torch.float16).to(dev)
-    b = torch.from_numpy(B.view(np.int16)).view(torch.float16).to(dev)
+    a, b = to_device(A, dev), to_device(B, dev)
     c = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     if args.variant >= 0 or args.raster > 0 or args.stream_k >= 0:
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         plan = G.gemm_f16_nt_plan_ex(w.M, w.N, w.K, args.variant, args.raster, args.stream_k)
         ws = G.workspace_for(plan, dev)
         step = lambda: G.gemm_f16_nt_run(plan, a, b, c, ws, stream=stream)  # noqa: E731
     else:
-        # the automatic plan through the workspace entry point (stream-K tail when it pays)
+        # the automatic plan through the workspace entry point (stream-K tail or split K when they pay)
         plan = G.gemm_f16_nt_plan(w.M, w.N, w.K)
         ws = G.workspace_for(plan, dev)
         step = lambda: G.gemm_f16_nt_ws(a, b, c, ws, stream=stream)  # noqa: E731
@@ -366,16 +480,14 @@ def main():
     if st != G.GEMM_OK:
         raise RuntimeError("kernel reported error word 0x%x" % code)
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(0)
     sampler.start()
     time.sleep(0.3)
     # One event pair around the K steps: events between launches would stand between two kernels
     # in the stream and stop a launch's set-up from overlapping its predecessor's tail.  Each step
-    # is exactly one launch of the GEMM kernel, back to back, so the average launch duration is
-    # the timed region over K (inter-kernel gaps included: conservative).
+    # is exactly one launch of the GEMM kernel (plus the reduction of a split-K plan), back to back,
+    # so the average launch duration is the timed region over K (inter-kernel gaps included).
     e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.mark_begin()
     with torch.cuda.stream(stream):
@@ -383,18 +495,15 @@ def main():
         for _ in range(args.steps):
             step()
         e_end.record(stream)
-    if dist is not None:
-        dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.mark_end()
-    clocks = sampler.stop()
     st, code = G.gemm_f16_take_device_error(stream)
     if st != G.GEMM_OK:
         raise RuntimeError("kernel reported error word 0x%x" % code)
     total_ms = e_begin.elapsed_time(e_end)
-    mean_launch_ms = total_ms / args.steps
-    value, total_ms = aggregate_throughput(total_ms, w.flops, args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
+    value = throughput(total_ms, w.flops, args.steps)
+    clocks = sampler.summary()
 
     # end to end through the host-buffer entry point: H2D of A and B from
     # pinned memory, the GEMM, D2H of C, every step
@@ -408,48 +517,38 @@ def main():
             G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, ws, stream=stream)
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if dist is not None:
-            dist.barrier()
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(e_steps):
             G.gemm_f16_nt_host(a_h, b_h, c_h, a, b, c, ws, stream=stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e_value, e_ms = aggregate_throughput(e0.elapsed_time(e1), w.flops, e_steps, dist, dev)
-        e2e = {"value": e_value, "unit": UNIT,
+        e2e = {"value": throughput(e0.elapsed_time(e1), w.flops, e_steps), "unit": UNIT,
                "h2d_bytes_per_step": 2 * (w.M * w.K + w.N * w.K), "d2h_bytes_per_step": 2 * w.M * w.N,
                "steps": e_steps}
 
-    if dist is not None:
-        dist.barrier()
-    if rank != 0:
-        dist.destroy_process_group()
-        return 0
-
     peaks = measured_peaks()
-    # The timed loop runs the kernel back to back for a long stretch under
-    # the board power cap, so the comparable denominator is the sustained
-    # (back-to-back, power-capped) cuBLAS bf16 figure; fp16 and bf16 have the
-    # same nominal tensor rate.  The burst figure is reported beside it.
-    burst = None
-    if peaks and "bf16_tflops_sustained" in peaks:
-        peak = float(peaks["bf16_tflops_sustained"])
-        peak_note = "of measured: cuBLAS bf16 sustained (back to back under the power cap); fp16 rate = bf16 rate"
-        burst = float(peaks.get("bf16_tflops", 0.0)) or None
-    else:
-        peak, peak_note = FALLBACK_PEAK_TFLOPS, "of fallback"
-    achieved = w.flops / (mean_launch_ms * 1e-3) / 1e12
-    roofline = {
-        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-        "peak_source": peak_note, "traffic": traffic_record(w.name, plan),
-        "algorithmic_bytes": w.algorithmic_bytes,
+    regime = timing_regime(total_ms, clocks)
+    roofline = tensor_roofline(value, regime, peaks)
+    roofline.update({
+        "traffic": traffic_record(w.name, plan), "algorithmic_bytes": w.algorithmic_bytes,
         "kernel": "gemm_f16_nt_wide_kernel" if plan.block_n > 256 else "gemm_f16_nt_kernel",
-        "frac_of_nominal_2250": achieved / NOMINAL_PEAK_TFLOPS,
-        "burst_peak": burst, "frac_of_burst": (achieved / burst) if burst else None,
-    }
+    })
+
+    workloads = None
+    if not args.no_workloads:
+        workloads = {}
+        for other in inputs.WORKLOADS:
+            if other.name == w.name:
+                workloads[other.name] = {"M": w.M, "N": w.N, "K": w.K, "ms": ms_per_step, "tflops": value,
+                                         "note": "the headline step above", "roofline": roofline}
+                continue
+            workloads[other.name] = time_workload(G, other, dev, stream, sampler, args.workload_launches,
+                                                  max(20, args.warmup), peaks)
+    sampler.stop()
+
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline:
         import oracle
         rate, secs, rows = cpu_oracle_rate(A, B, target_s=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
@@ -457,18 +556,17 @@ def main():
     cfg = workload_config(w)
     cfg["plan"] = {k: v for k, v in plan.as_dict().items() if k in (
         "variant", "cta_group", "block_m", "block_n", "stages", "raster_width", "grid", "stream_k", "dp_tiles",
-        "workspace_bytes")}
+        "workspace_bytes", "split_k", "k_rotate")}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
-        "frac_of_nominal_peak": value / world / NOMINAL_PEAK_TFLOPS,
+        "frac_of_nominal_peak": value / NOMINAL_PEAK_TFLOPS,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": args.steps * (2 if plan.split_k > 1 else 1),  # a split-K plan adds its reduction
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
     return 0
 
 
