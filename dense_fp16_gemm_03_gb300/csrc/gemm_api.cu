@@ -35,12 +35,53 @@ constexpr int kMaxDevices = 64;
 
 // ---------------------------------------------------- per-device state
 
+// Identity of the calling thread's current CUDA context (cuCtxGetCurrent +
+// cuCtxGetId through the runtime's driver entry points).  Per-device state
+// below is kept per context: after cudaDeviceReset the primary context, the
+// module and every address looked up in it are new, so state made for an
+// earlier context is made again instead of reused.
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+
+gemm_status_t current_context_id(unsigned long long *id)
+{
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PfnCtxGetCurrent>(f);
+        else
+            cudaGetLastError();
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PfnCtxGetId>(f);
+        else
+            cudaGetLastError();
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return GEMM_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    // no context yet on this thread: let the runtime make the device's primary context current
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+        if (cudaFree(nullptr) != cudaSuccess || g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+    }
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 struct DeviceInfo {
     bool ready = false;
+    unsigned long long ctx_id = 0;  // the context the entries below were made in
     bool arch_ok = false;
     int num_sms = 0;
     int max_clusters[kNumVariants] = {};
-    bool attr_set[kNumVariants] = {};
+    uint32_t *error_word = nullptr;  // device address of g_gemm_f16_error_word in that context
 };
 
 std::mutex g_mutex;
@@ -53,9 +94,14 @@ gemm_status_t device_info(DeviceInfo **out)
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
+    unsigned long long ctx = 0;
+    gemm_status_t st = current_context_id(&ctx);
+    if (st != GEMM_OK) return st;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo &d = g_devices[dev];
-    if (!d.ready) {
+    if (!d.ready || d.ctx_id != ctx) {
+        DeviceInfo made;
+        made.ctx_id = ctx;
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -63,9 +109,9 @@ gemm_status_t device_info(DeviceInfo **out)
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
-        d.arch_ok = (major == 10 && minor == 3);
-        d.num_sms = sms;
-        if (d.arch_ok) {
+        made.arch_ok = (major == 10 && minor == 3);
+        made.num_sms = sms;
+        if (made.arch_ok) {
             for (int v = 0; v < kNumVariants; ++v) {
                 const Variant &var = kVariants[v];
                 if (cudaFuncSetAttribute(var.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, var.smem) !=
@@ -73,9 +119,8 @@ gemm_status_t device_info(DeviceInfo **out)
                     cudaGetLastError();
                     return GEMM_ERR_CUDA;
                 }
-                d.attr_set[v] = true;
                 const int cs = var.cg * var.mc;
-                d.max_clusters[v] = sms / cs;
+                made.max_clusters[v] = sms / cs;
                 if (cs > 1) {
                     cudaLaunchConfig_t cfg;
                     memset(&cfg, 0, sizeof(cfg));
@@ -91,19 +136,36 @@ gemm_status_t device_info(DeviceInfo **out)
                     cfg.numAttrs = 1;
                     int clusters = 0;
                     if (cudaOccupancyMaxActiveClusters(&clusters, var.fn, &cfg) == cudaSuccess && clusters > 0)
-                        d.max_clusters[v] = clusters;
+                        made.max_clusters[v] = clusters;
                     else
                         cudaGetLastError();
                 }
             }
+            void *err_ptr = nullptr;
+            if (cudaGetSymbolAddress(&err_ptr, g_gemm_f16_error_word) != cudaSuccess || err_ptr == nullptr) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            made.error_word = static_cast<uint32_t *>(err_ptr);
         }
-        d.ready = true;
+        made.ready = true;
+        d = made;
     }
     *out = &d;
     return d.arch_ok ? GEMM_OK : GEMM_ERR_ARCH;
 }
 
 // ---------------------------------------------------------- validation
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return dev;
+}
 
 bool aligned16(const void *p)
 {
@@ -488,6 +550,19 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
     }
     const Variant &var = kVariants[plan.variant];
+    if (var.mc > 1) {
+        // Cluster multicast loads deliver one copy of a tile to several CTAs of this GPU; they are
+        // only used on this GPU's own device memory (never on a peer's or on host-mapped memory).
+        const int cur = current_device();
+        for (const void *ptr : {a, b}) {
+            cudaPointerAttributes at;
+            if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_INVALID_ARG;
+            }
+            if (at.type != cudaMemoryTypeDevice || at.device != cur) return GEMM_ERR_INVALID_ARG;
+        }
+    }
 
     KernelParams params;
     memset(&params, 0, sizeof(params));
@@ -517,12 +592,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     }
     params.skip_fill = skip_fill;
     params.wait_limit = wait_limit;
-    void *err_ptr = nullptr;
-    if (cudaGetSymbolAddress(&err_ptr, g_gemm_f16_error_word) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    params.error_word = static_cast<uint32_t *>(err_ptr);
+    params.error_word = dev->error_word;
     if (var.launch(plan, params, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -559,6 +629,12 @@ const char *gemm_f16_status_string(gemm_status_t s)
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime call failed";
     }
     return "unknown gemm_status_t";
+}
+
+// The name the boundary's specification gives the same function.
+const char *gemm_status_string(gemm_status_t s)
+{
+    return gemm_f16_status_string(s);
 }
 
 int32_t gemm_f16_variant_count(void)
@@ -628,6 +704,7 @@ constexpr int64_t kHostChunkRowsMin = 1024;
 
 struct HostPipe {
     bool ready = false;
+    unsigned long long ctx_id = 0;  // the context the streams and events belong to
     cudaStream_t in = nullptr, out = nullptr;  // inbound and outbound copy streams
     cudaEvent_t start = nullptr, in_done = nullptr, out_done = nullptr;
     cudaEvent_t landed[kHostChunksMax] = {};    // chunk i's rows of A (and all of B) are on the device
@@ -646,9 +723,14 @@ gemm_status_t host_pipe(HostPipe **out)
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
+    unsigned long long ctx = 0;
+    gemm_status_t st = current_context_id(&ctx);
+    if (st != GEMM_OK) return st;
     HostPipe &hp = g_pipes[dev];
-    if (!hp.ready) {
+    if (!hp.ready || hp.ctx_id != ctx) {
+        // (streams and events of an earlier, reset context are gone with it)
         HostPipe made;
+        made.ctx_id = ctx;
         bool ok = cudaStreamCreateWithFlags(&made.in, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaStreamCreateWithFlags(&made.out, cudaStreamNonBlocking) == cudaSuccess;
         cudaEvent_t *events[3 + 2 * kHostChunksMax] = {&made.start, &made.in_done, &made.out_done};
@@ -932,10 +1014,17 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_F16_STATIC
 
 namespace {
 
-void *g_noalloc_ptr[kMaxDevices] = {};
+struct NoallocScratch {
+    unsigned long long ctx_id = 0;  // the context the address was looked up in
+    void *ptr = nullptr;
+};
+NoallocScratch g_noalloc[kMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (host code must not pass the symbol itself to a kernel).
+// Device address of g_noalloc_scratch on the current device, looked up with
+// that device current once per context (host code must not pass the symbol
+// itself to a kernel: in host code it names a host-side stand-in).  After
+// cudaDeviceReset the module is loaded anew and the address is looked up
+// again.
 gemm_status_t noalloc_scratch(void **out)
 {
     int dev = 0;
@@ -943,16 +1032,21 @@ gemm_status_t noalloc_scratch(void **out)
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
+    unsigned long long ctx = 0;
+    gemm_status_t st = current_context_id(&ctx);
+    if (st != GEMM_OK) return st;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocScratch &s = g_noalloc[dev];
+    if (s.ptr == nullptr || s.ctx_id != ctx) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
-        g_noalloc_ptr[dev] = ptr;
+        s.ctx_id = ctx;
+        s.ptr = ptr;
     }
-    *out = g_noalloc_ptr[dev];
+    *out = s.ptr;
     return GEMM_OK;
 }
 

@@ -72,7 +72,7 @@ class Plan(ctypes.Structure):
 
 # every symbol the public header declares
 EXPORTED = [
-    "gemm_f16_status_string", "gemm_f16_variant_count", "gemm_f16_variant_info",
+    "gemm_f16_status_string", "gemm_status_string", "gemm_f16_variant_count", "gemm_f16_variant_info",
     "gemm_f16_nt_plan", "gemm_f16_nt_plan_for", "gemm_f16_nt_plan_for_clusters", "gemm_f16_nt_plan_ex",
     "gemm_f16_nt_workspace_size",
     "gemm_f16_nt", "gemm_f16_nt_ws", "gemm_f16_nt_run", "gemm_f16_nt_host",
@@ -97,6 +97,7 @@ def lib():
     P = ctypes.POINTER(Plan)
     sig = {
         "gemm_f16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "gemm_f16_variant_count": (i32, []),
         "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32, pi32]),
         "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),

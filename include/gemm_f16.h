@@ -22,6 +22,18 @@
  * on `stream`; a, b are only read; c is fully overwritten (no beta, no
  * accumulate).  Overlap of c with a or b is undefined.
  *
+ * Host-side state per device (SM and cluster counts, the error word's
+ * device address, the copy streams of gemm_f16_nt_host) is kept for the
+ * context it was made in and made again when the current context changes,
+ * so a cudaDeviceReset between calls is safe; a reset that races with a
+ * call on another thread is not.
+ *
+ * One GPU per call: a, b and c are memory of the current device.  The
+ * variants that share one operand tile between the CTAs of a cluster by
+ * multicast (see gemm_f16_variant_info) check this and return
+ * GEMM_ERR_INVALID_ARG for any other pointer (a peer GPU's memory, host
+ * memory); the library has no multi-GPU path.
+ *
  * Errors: every entry point validates its arguments on the host before any
  * launch and returns a status code; it never exits or aborts the process.
  *   - m, n, k >= 0.  m == 0 or n == 0 is a no-op.  k == 0 writes C := 0
@@ -130,8 +142,11 @@ typedef struct gemm_f16_plan {
  * operand swap only (0-4, 11, 12).
  */
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).  No
+ * counterpart on the pages (their only error convention is the day78 page's
+ * check-and-exit macro); gemm_status_string is the same function. */
 const char *gemm_f16_status_string(gemm_status_t status);
+const char *gemm_status_string(gemm_status_t status);
 
 /* Number of compiled kernel variants, and the shape of one of them: CTAs
  * per MMA (cta_group), tile N of one CTA or pair (a wide tile's two MMAs
@@ -150,7 +165,10 @@ gemm_status_t gemm_f16_variant_info(int32_t variant, int32_t *cta_group, int32_t
  * Plan for the current CUDA device: validates the shape, checks the device
  * is compute capability 10.3, picks a variant, the grid and whether a
  * stream-K tail pays (then workspace_bytes > 0).  Host only, allocates
- * nothing, launches nothing.
+ * nothing, launches nothing.  The grid of tiles is the cdiv(m, BM) x
+ * cdiv(n, BN) grid of "1. WGMMA", section "The Full Kernel"; the walk over
+ * it is the rasterization of "4. Pipeline Abstraction and Two Consumer Warp
+ * Groups", section "Tile Rasterization".
  */
 gemm_status_t gemm_f16_nt_plan(int64_t m, int64_t n, int64_t k, gemm_f16_plan_t *out);
 
@@ -193,19 +211,23 @@ gemm_status_t gemm_f16_nt_plan_ex(int64_t m, int64_t n, int64_t k, int32_t varia
 
 /* Device workspace (bytes) gemm_f16_nt_ws needs for this shape on the
  * current device (the stream-K partial tiles and flags, or the split-K
- * parts); 0 when the chosen plan needs none. */
+ * parts); 0 when the chosen plan needs none.  No counterpart on the pages:
+ * their kernels keep each tile's whole K loop in one thread block. */
 gemm_status_t gemm_f16_nt_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes);
 
 /*
- * C = A . B^T on `stream`.  a: device pointer to M*K fp16, b: device pointer
- * to N*K fp16, c: device pointer to M*N fp16.  Plans automatically among the
- * plans that need no workspace (no stream-K tail, no split K).
+ * C = A . B^T on `stream`: the product of "1. WGMMA: Hopper's Asynchronous
+ * Tensor Core", section "The Full Kernel" (its matmul(m_size, n_size,
+ * k_size, a_ptr, b_ptr, c_ptr) with a stream added).  a: device pointer to
+ * M*K fp16, b: device pointer to N*K fp16, c: device pointer to M*N fp16.
+ * Plans automatically among the plans that need no workspace (no stream-K
+ * tail, no split K).
  */
 gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b,
                           void *c, gemm_stream_t stream);
 
-/* As gemm_f16_nt with a caller-owned device workspace of ws_bytes bytes,
- * 256-byte aligned: uses the automatic plan, with a stream-K tail or split K
+/* The product of gemm_f16_nt ("1. WGMMA", "The Full Kernel"), with a
+ * caller-owned device workspace of ws_bytes bytes, 256-byte aligned: uses the automatic plan, with a stream-K tail or split K
  * when it pays.  workspace may be NULL/0 when gemm_f16_nt_workspace_size reports 0;
  * too small -> GEMM_ERR_WORKSPACE, misaligned -> GEMM_ERR_ALIGNMENT.  Calls
  * that share one workspace must not overlap on the GPU. */
@@ -214,12 +236,15 @@ gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, con
 
 /* Launch a given plan (from any plan query, made for the current device's
  * SM count; either layout, c then being the plan's C or D).  The plan is
- * re-validated. */
+ * re-validated.  Computes the product of "1. WGMMA", "The Full Kernel" (or,
+ * for layout 1, of "wgmma_gemm.cu"); the plan's fields only choose how. */
 gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c,
                               void *workspace, size_t ws_bytes, gemm_stream_t stream);
 
 /*
- * End-to-end form for host-resident data: copies a_host (M*K fp16) and
+ * End-to-end form for host-resident data (the host-to-device copies,
+ * product and copy back that "wgmma_gemm.cu" does in its main, here
+ * overlapped): copies a_host (M*K fp16) and
  * b_host (N*K fp16) into the caller's device buffers a_dev / b_dev, runs
  * the GEMM into c_dev (automatic plan; the workspace, which may be NULL/0,
  * serves a stream-K tail or split K when it is large enough), and copies c_dev back to

@@ -27,7 +27,7 @@ def L():
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "gemm_f16.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gemm_\w+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -47,6 +47,7 @@ def test_static_scratch_size_matches_header(L):
 def test_status_strings(L):
     for s in range(9):
         assert G.status_string(s).startswith("GEMM_")
+        assert L.gemm_status_string(s) == L.gemm_f16_status_string(s)
     assert "unknown" in G.status_string(99)
 
 
