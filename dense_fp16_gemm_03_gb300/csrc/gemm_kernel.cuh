@@ -85,6 +85,7 @@ enum : uint32_t {
     kErrWaitAccFull = 4,
     kErrWaitDrain = 5,
     kErrWaitPartial = 6,
+    kErrWaitRingDrain = 7,   // after an abort, a ring stage's loads did not all land in time
 };
 
 struct KernelParams {
@@ -138,7 +139,8 @@ struct KernelCfg {
     static constexpr int kOffBar = kOffStore + kEpiWarps * EPI * kStoreBufBytes;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kSmemUsed = kOffAbort + 4;
+    static constexpr int kOffFills = kOffAbort + 4;  // ring fills the producer walked (read by the abort drain)
+    static constexpr int kSmemUsed = kOffFills + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kAccCols = (BN + 63) / 64 * 64;  // accumulator buffer stride (64-column aligned)
     static constexpr int kTmemCols = (2 * kAccCols <= 128) ? 128 : (2 * kAccCols <= 256 ? 256 : 512);
@@ -185,6 +187,52 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr)
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major = false)
 {
     return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// After an abort, make sure no TMA load can still write into the ring once
+// the CTAs exit.  Run by one thread of every CTA whose full barriers count
+// the ring's bytes (every CTA for single-CTA MMAs, the first CTA of each
+// pair otherwise), between two cluster barriers of the teardown.
+//   fills[x]:  ring fills the producer of cluster CTA x walked (loads issued
+//              for each, except the test hook's skipped fill of block 0);
+//   share(x):  bytes the loads of one fill by CTA x complete on this CTA's
+//              full barrier; stage_tx the bytes this CTA arms per fill.
+// A producer issues fill f only after every MMA consumed fill f - STAGES of
+// that stage, so only the last STAGES fills can have loads in flight.  For
+// each: bytes armed here but never issued are completed by hand, a fill
+// never armed here whose loads were issued elsewhere is armed now for just
+// those bytes, and then the stage's phase is awaited (bounded).
+template <int STAGES, int CS, class Share>
+__device__ __forceinline__ void drain_ring(uint32_t bar_full0, const uint32_t (&fills)[CS], uint32_t self, uint32_t first_block,
+                           uint32_t stage_tx, Share share, const KernelParams &p)
+{
+    uint32_t fmax = 0;
+#pragma unroll
+    for (int x = 0; x < CS; ++x) fmax = fills[x] > fmax ? fills[x] : fmax;
+    const uint32_t f0 = fmax > uint32_t(STAGES) ? fmax - uint32_t(STAGES) : 0u;
+    for (uint32_t f = f0; f < fmax; ++f) {
+        auto issued = [&](uint32_t x) { return f < fills[x] && !(first_block + x == 0u && f == p.skip_fill); };
+        uint32_t landing = 0;
+#pragma unroll
+        for (int x = 0; x < CS; ++x)
+            if (issued(uint32_t(x))) landing += share(uint32_t(x));
+        const uint32_t bar = bar_full0 + 8u * (f % uint32_t(STAGES));
+        if (issued(self)) {
+            if (stage_tx > landing) ptx::mbar_complete_tx(bar, stage_tx - landing);
+        } else if (landing > 0) {
+            ptx::mbar_arrive_expect_tx(bar, landing);
+        } else {
+            continue;
+        }
+        const uint32_t parity = (f / uint32_t(STAGES)) & 1u;
+        const long long t0 = clock64();
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (clock64() - t0 > p.wait_limit) {
+                atomicCAS(p.error_word, 0u, kErrWaitRingDrain | (blockIdx.x << 8));
+                break;
+            }
+        }
+    }
 }
 
 // Bounded wait on phase `parity` of the barrier at `bar` (cluster-scope
@@ -257,6 +305,44 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// The teardown's abort drain (see drain_ring), run by one thread of every
+// CTA that owns full barriers, between two cluster barriers: if any CTA of
+// the cluster gave up a wait, wait for the ring loads still in flight.  Kept
+// out of line, and recomputing its addresses, so that it costs the main
+// loops no registers.
+template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI>
+__device__ __noinline__ void nt_abort_drain(const KernelParams &p)
+{
+    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>;
+    constexpr int CS = Cfg::kCS;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t cta_rank = (CS > 1) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t pair = cta_rank / CG;
+    uint32_t fills[CS];
+    bool aborted = false;
+    if constexpr (CS > 1) {
+#pragma unroll
+        for (int x = 0; x < CS; ++x) {
+            aborted |= ptx::ld_shared_cluster_u32(ptx::map_to_rank(base + Cfg::kOffAbort, uint32_t(x))) != 0u;
+            fills[x] = ptx::ld_shared_cluster_u32(ptx::map_to_rank(base + Cfg::kOffFills, uint32_t(x)));
+        }
+    } else {
+        aborted = *reinterpret_cast<volatile uint32_t *>(smem_raw + (base - raw) + Cfg::kOffAbort) != 0u;
+        fills[0] = *reinterpret_cast<volatile uint32_t *>(smem_raw + (base - raw) + Cfg::kOffFills);
+    }
+    if (!aborted) return;
+    // bytes one fill of cluster CTA x lands on this CTA's full barriers (see the producer)
+    auto share = [&](uint32_t x) -> uint32_t {
+        if constexpr (Cfg::kAMC) return uint32_t(Cfg::kASlice * 128) + (x == cta_rank ? uint32_t(Cfg::kBBytes) : 0u);
+        else if constexpr (MC == 1) return uint32_t(Cfg::kABytes + Cfg::kBBytes);
+        else return ((x / CG) == pair ? uint32_t(Cfg::kABytes) : 0u) + uint32_t(Cfg::kBSlice * 128);
+    };
+    drain_ring<STAGES, CS>(base + Cfg::kOffBar, fills, cta_rank, blockIdx.x - cta_rank, uint32_t(Cfg::kStageTx),
+                           share, p);
+}
+
 template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ KernelParams p)
 {
@@ -288,12 +374,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     const uint32_t bar_drain = base + Cfg::kOffBar + 8u * (2 * STAGES + 4);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffTmemSlot);
+    volatile uint32_t *fills_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffFills);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full(s), 1);
             ptx::mbar_init(bar_empty(s), MC);  // released by the MMA issuer of every pair
         }
+        *fills_slot = 0u;
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_acc_full(b), 1);
             ptx::mbar_init(bar_acc_empty(b), kEpiWarps * CG);
@@ -392,7 +480,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 }
                 return true;
             });
-            if (!ok) __nanosleep(100000);  // let copies already issued land before teardown
+            *fills_slot = fills;  // read by the teardown's abort drain
+            (void)ok;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -657,6 +746,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     if constexpr (CS > 1) ptx::cluster_sync();
     else __syncthreads();
     ptx::tc_fence_after_sync();
+    // Between two cluster barriers every CTA of the cluster is still running, so the owners of full
+    // barriers may read the other CTAs' flags: after an abort anywhere in the cluster they wait for
+    // the ring loads still in flight before any CTA exits.
+    if (threadIdx.x == 0 && (CG == 1 || leader))
+        nt_abort_drain<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>(p);
+    if constexpr (CS > 1) ptx::cluster_sync();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
 }
 

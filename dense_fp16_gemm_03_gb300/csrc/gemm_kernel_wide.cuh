@@ -1,7 +1,7 @@
 // Wide-tile variant of the persistent sm_103a kernel: a CTA pair computes a
 // 256 x (2 HALF_N) tile of C[M,N] = A[M,K] . B[N,K]^T (fp16 in, fp32
 // accumulate, fp16 out) as two cta_group::2 MMAs of N = HALF_N per K step
-// (HALF_N = 256: 256 x 512 tiles; 224: 256 x 448).
+// (HALF_N = 256: 256 x 512 tiles; 224: 256 x 448; 160: 256 x 320).
 //
 // Why a wider tile: every byte of A and B reaches a CTA's shared memory
 // through the SM's port on the L2 crossbar.  On GB300 that delivery measured
@@ -61,7 +61,8 @@ struct WideCfg {
     static constexpr int kOffBar = kOffStore + kWideEpiWarps * kStoreBufBytes;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kSmemUsed = kOffAbort + 4;
+    static constexpr int kOffFills = kOffAbort + 4;  // ring fills the producer walked (read by the abort drain)
+    static constexpr int kSmemUsed = kOffFills + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kTmemCols = 512;
     static_assert(kBSubBytes % 1024 == 0, "B sub-tiles stay 1024-byte aligned for the 128-byte swizzle");
@@ -77,6 +78,29 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t row_addr, uint32_t row,
     for (int j = 0; j < 8; ++j)
         ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (row & 7u)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
                           w[4 * j + 3]);
+}
+
+// The teardown's abort drain of the wide kernel (see drain_ring), run by the
+// pair's first CTA between two cluster barriers: if either CTA gave up a
+// wait, wait for the ring loads still in flight.  Kept out of line, and
+// recomputing its addresses, so that it costs the main loops no registers.
+template <int STAGES, int HALF_N>
+__device__ __noinline__ void wide_abort_drain(const KernelParams &p)
+{
+    using Cfg = WideCfg<STAGES, HALF_N>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t abort_addr = base + Cfg::kOffAbort;
+    if (ptx::ld_shared_cluster_u32(ptx::map_to_rank(abort_addr, 0u)) == 0u &&
+        ptx::ld_shared_cluster_u32(ptx::map_to_rank(abort_addr, 1u)) == 0u)
+        return;
+    const uint32_t fills_addr = base + Cfg::kOffFills;
+    const uint32_t fills[2] = {ptx::ld_shared_cluster_u32(ptx::map_to_rank(fills_addr, 0u)),
+                               ptx::ld_shared_cluster_u32(ptx::map_to_rank(fills_addr, 1u))};
+    // each CTA's loads of one fill (its A rows, its two B sub-tiles) land on the leader's barrier
+    drain_ring<STAGES, 2>(base + Cfg::kOffBar, fills, 0u, blockIdx.x, uint32_t(Cfg::kStageTx),
+                          [](uint32_t) { return uint32_t(Cfg::kABytes + Cfg::kBBytes); }, p);
 }
 
 template <int STAGES, int HALF_N>
@@ -103,12 +127,14 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
     const uint32_t bar_drain = base + Cfg::kOffBar + 8u * (2 * STAGES + 2);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffTmemSlot);
+    volatile uint32_t *fills_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffFills);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full(s), 1);
             ptx::mbar_init(bar_empty(s), 1);
         }
+        *fills_slot = 0u;
         ptx::mbar_init(bar_acc_full, 1);
         ptx::mbar_init(bar_acc_empty, kWideEpiWarps * CS);
         ptx::mbar_init(bar_drain, 1);
@@ -170,7 +196,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                 }
                 return true;
             });
-            if (!ok) __nanosleep(100000);  // let copies already issued land before teardown
+            *fills_slot = fills;  // read by the teardown's abort drain
+            (void)ok;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -326,6 +353,10 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
     ptx::tc_fence_before_sync();
     ptx::cluster_sync();
     ptx::tc_fence_after_sync();
+    // Both CTAs stay until the second barrier, so the first CTA may read the second's flags: after an
+    // abort in either, it waits for every ring load still in flight before either CTA exits.
+    if (threadIdx.x == 0 && leader) wide_abort_drain<STAGES, HALF_N>(p);
+    ptx::cluster_sync();
     if (warp == 1) ptx::tmem_dealloc<2>(tmem_base, Cfg::kTmemCols);
 }
 

@@ -66,6 +66,13 @@ __device__ __forceinline__ void mbar_arrive_cluster_signal(uint32_t bar_cluster)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
+// Complete `bytes` of the barrier's expected transaction count without a
+// copy: for bytes that were expected but will never arrive.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -125,6 +132,20 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
     uint32_t out;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
     return out;
+}
+
+// 32-bit load / store of shared memory named by a shared::cluster address
+// (possibly in another CTA of the cluster).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync()
