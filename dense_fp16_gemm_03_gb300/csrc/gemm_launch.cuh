@@ -117,6 +117,8 @@ const Variant kVariants[] = {
     // wide tiles on a CTA pair, one accumulator filling tensor memory (no stream-K tail)
     GEMM_VARIANT_WIDE(4, 256),  // 15: 256 x 512
     GEMM_VARIANT_WIDE(4, 224),  // 16: 256 x 448 (fills the last wave where N / 512 would leave it idle)
+    GEMM_VARIANT_WIDE(5, 160),  // 17: 256 x 320, five stages (4096^3: 208 tiles, 2.7 waves, where 512 columns
+                                //     make 128 tiles, 1.7 waves)
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 

@@ -7,7 +7,8 @@ plans that need scratch (a stream-K tail, split K) with that scratch taken
 from an array built into the library, so its results must agree with the
 workspace entry point
 (gemm_f16_nt_ws with a caller-allocated workspace) within the parity bound
-the other tests use, on consecutive calls that reuse that one array.
+the other tests use, on consecutive calls that reuse that one array -- and,
+like every other entry point, with the CPU oracle.
 
 This file is collected last on purpose: a failure here leaves every other
 test already run.
@@ -24,8 +25,7 @@ from dense_fp16_gemm_03_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def _within_bound(got_bits, ref_bits, A, B):
-    _, absum = oracle.gemm_nt(A, B)
+def _within_bound(got_bits, ref_bits, absum):
     rep = oracle.check_parity(got_bits, ref_bits, absum, index_shape=ref_bits.shape)
     assert rep.ok, repr(rep)
 
@@ -42,9 +42,10 @@ def test_noalloc_matches_workspace_entry_point_twice(shape, dist):
     a, b = to_dev(A), to_dev(B)
 
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    c_ref = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    G.gemm_f16_nt_ws(a, b, c_ref, ws)
-    ref_bits = from_dev_bits(c_ref)
+    c_ws = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    G.gemm_f16_nt_ws(a, b, c_ws, ws)
+    ws_bits = from_dev_bits(c_ws)
+    oracle_bits, absum = oracle.gemm_nt(A, B)
 
     for call in range(2):
         c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
@@ -52,6 +53,8 @@ def test_noalloc_matches_workspace_entry_point_twice(shape, dist):
         st, code = G.gemm_f16_take_device_error()
         assert st == G.GEMM_OK, "call %d: device error word 0x%x" % (call, code)
         got_bits = from_dev_bits(c)
-        _within_bound(got_bits, ref_bits, A, B)
+        _within_bound(got_bits, ws_bits, absum)       # against the workspace entry point
+        _within_bound(got_bits, oracle_bits, absum)   # against the oracle
         if dist == "eighths":              # integer-valued sums are exact in any order
-            assert np.array_equal(got_bits, ref_bits)
+            assert np.array_equal(got_bits, ws_bits)
+            assert np.array_equal(got_bits, oracle_bits)
