@@ -269,10 +269,13 @@ __device__ __forceinline__ uint64_t sk_begin(const KernelParams &p, uint32_t w, 
 // Every role walks the same sequence of segments (tile, [k_lo, k_hi)):
 // data-parallel tiles first, then this cluster's stream-K range; with split-K
 // instead the parts u = tile * split_k + s, s-th of split_k equal K ranges,
-// one after another per cluster.  f returns false to stop early (abort).  A kernel that never runs
-// split-K plans instantiates it with kSplitK = false.
-template <bool kSplitK = true, class F>
-__device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t worker, uint32_t workers, F &&f)
+// one after another per cluster.  f_dp receives the data-parallel tiles,
+// f_sk the stream-K segments (and split-K parts); either returns false to
+// stop early (abort).  A kernel that never runs split-K plans instantiates
+// it with kSplitK = false.
+template <bool kSplitK = true, class FD, class FS>
+__device__ __forceinline__ void for_each_segment2(const KernelParams &p, uint32_t worker, uint32_t workers, FD &&f_dp,
+                                                  FS &&f_sk)
 {
     if (kSplitK && p.split_k > 1) {
         const uint64_t units = uint64_t(p.num_tiles) * p.split_k;
@@ -280,12 +283,12 @@ __device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t
             const uint32_t tile = uint32_t(u / p.split_k), part = uint32_t(u % p.split_k);
             const uint32_t k_lo = uint32_t(uint64_t(part) * p.k_blocks / p.split_k);
             const uint32_t k_hi = uint32_t(uint64_t(part + 1) * p.k_blocks / p.split_k);
-            if (!f(tile, k_lo, k_hi)) return;
+            if (!f_sk(tile, k_lo, k_hi)) return;
         }
         return;
     }
     for (uint32_t tile = worker; tile < p.dp_tiles; tile += workers)
-        if (!f(tile, 0u, p.k_blocks)) return;
+        if (!f_dp(tile, 0u, p.k_blocks)) return;
     if (p.sk_iters == 0) return;
     uint64_t it = sk_begin(p, worker, workers);
     const uint64_t end = sk_begin(p, worker + 1, workers);
@@ -294,9 +297,16 @@ __device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t
         const uint32_t k_lo = uint32_t(it - u * p.k_blocks);
         const uint64_t left = end - it;
         const uint32_t k_hi = (left >= uint64_t(p.k_blocks - k_lo)) ? p.k_blocks : k_lo + uint32_t(left);
-        if (!f(p.dp_tiles + uint32_t(u), k_lo, k_hi)) return;
+        if (!f_sk(p.dp_tiles + uint32_t(u), k_lo, k_hi)) return;
         it += k_hi - k_lo;
     }
+}
+
+// The same walk with one function for every segment.
+template <bool kSplitK = true, class F>
+__device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t worker, uint32_t workers, F &&f)
+{
+    for_each_segment2<kSplitK>(p, worker, workers, f, f);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits)

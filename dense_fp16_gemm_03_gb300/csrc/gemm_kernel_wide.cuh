@@ -29,8 +29,12 @@
 //               last 32-column box.
 //
 // The pipeline, the raster order, the K rotation, the ragged-edge rules and
-// the bounded waits are those of gemm_kernel.cuh; this variant has neither a
-// stream-K tail nor split-K (its plans are always data-parallel).
+// the bounded waits are those of gemm_kernel.cuh.  A stream-K tail covers only
+// the partial last wave (every whole wave stays data-parallel, because a
+// partial of a 256 x 512 tile is 512 KB): a segment that ends a tile's K walk
+// publishes its fp32 partial straight from tensor memory, and the tile's
+// owner, whose segment is the last of its range, adds the partials chunk by
+// chunk on the way out.  There is no split-K.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -57,7 +61,9 @@ struct WideCfg {
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
-    static constexpr int kNumBars = 2 * STAGES + 3;  // full, empty, acc_full, acc_empty, drain
+    // full, empty, acc_full, acc_empty, drain, then two per epilogue warp for the stream-K owner's
+    // partial pieces
+    static constexpr int kNumBars = 2 * STAGES + 3 + 2 * kWideEpiWarps;
     static constexpr int kOffBar = kOffStore + kWideEpiWarps * kStoreBufBytes;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -66,6 +72,7 @@ struct WideCfg {
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kTmemCols = 512;
     static_assert(kBSubBytes % 1024 == 0, "B sub-tiles stay 1024-byte aligned for the 128-byte swizzle");
+    static_assert(STAGES * (kABytes + kBBytes) >= kWideEpiWarps * 2 * 4096, "partial pieces land in the idle ring");
     static_assert(kHalfCol + kHalfN <= kTmemCols, "both accumulator halves fit tensor memory");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
@@ -138,6 +145,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         ptx::mbar_init(bar_acc_full, 1);
         ptx::mbar_init(bar_acc_empty, kWideEpiWarps * CS);
         ptx::mbar_init(bar_drain, 1);
+        for (int b = 0; b < 2 * kWideEpiWarps; ++b) ptx::mbar_init(bar_drain + 8u * (1 + b), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&p.tmap_a);
@@ -248,8 +256,208 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         const uint32_t row_addr = buf + lane * 128u;
         const uint32_t t_col = tmem_base + ((quarter * 32u) << 16) + half * uint32_t(Cfg::kHalfCol);
         constexpr int kHeld = Cfg::kFullChunks - 1;
+        // Stream-K partial tile of one CTA in the workspace: 128 rows x kBN fp32.  Warp piece
+        // (half, quarter) = 32 rows x HALF_N columns at (half * 4 + quarter) * 32 * HALF_N; inside it,
+        // 32-column chunk c, float4 j (columns 32c + 4j ..) of lane l at ((c * 8 + j) * 32 + l) * 4,
+        // so every warp-wide 16-byte access is one contiguous 512-byte run.
+        constexpr uint32_t kSlotFloats = 128u * uint32_t(Cfg::kBN);
         uint32_t acc_phase = 0;
-        for_each_segment<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
+        // a stream-K segment of the tail: publish its fp32 partial (it ends a tile's K walk) or finish a
+        // tile as its owner (it starts the tile's K walk; the last segment of this cluster's range)
+        auto sk_segment = [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
+            uint32_t mb, nb;
+            raster_coord(p.raster, tile, mb, nb);
+            const uint32_t row0 = mb * Cfg::kBM + pair_rank * 128u + quarter * 32u;
+            const uint32_t col0 = nb * Cfg::kBN + half * uint32_t(Cfg::kHalfN);
+            const bool ok = wait_bounded<CS>(bar_acc_full, acc_phase, p, abort_flag, kErrWaitAccFull);
+            // the owner meets the other epilogue warps at named barrier 1, so the decision to stop
+            // must be the same in all eight warps
+            if (!ptx::named_barrier_and(1, 32 * kWideEpiWarps, ok)) return false;
+            acc_phase ^= 1u;
+            ptx::tc_fence_after_sync();
+            const bool live = (row0 < p.m) && (col0 < p.n);
+            if (k_lo != 0u) {
+                // ---- publish: this segment ends the tile's K walk; its fp32 partial goes to this
+                // CTA's workspace slot for the tile's owner to add, then the flag gets the stamp
+                const uint32_t piece = (half * 4u + quarter) * 32u * uint32_t(Cfg::kHalfN) + lane * 4u;
+                float *slot = p.partials + size_t(blockIdx.x) * kSlotFloats + piece;
+                if (live) {
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::kHalfN / 32; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32_wait(t_col + uint32_t(32 * c), r);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            ptx::st_global_cg_f4(slot + (c * 8 + j) * 128, __uint_as_float(r[4 * j]),
+                                                 __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                                                 __uint_as_float(r[4 * j + 3]));
+                    }
+                }
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster_signal(ptx::map_to_rank(bar_acc_empty, 0u));
+                __threadfence();
+                ptx::named_barrier_sync(1, 32 * kWideEpiWarps);
+                if (threadIdx.x == 64u) ptx::st_release_gpu_u64(p.flags + blockIdx.x, p.sk_stamp);
+                return true;
+            }
+            {
+                // ---- owner of a tile (always the last segment of this cluster's range): wait
+                // for the clusters that hold the rest of the tile's K walk, then add their partials
+                // to the accumulator chunk by chunk on the way out; tensor memory is released at the
+                // end (nothing of this cluster waits for it)
+                const uint64_t tile_end = uint64_t(tile - p.dp_tiles + 1) * p.k_blocks;
+                const uint32_t first_w = cluster_id + 1;
+                uint32_t last_w = first_w;
+                while (last_w < num_clusters && sk_begin(p, last_w, num_clusters) < tile_end) ++last_w;
+                if (threadIdx.x == 64u) {
+                    for (uint32_t w = first_w; w < last_w; ++w) {
+                        if (sk_begin(p, w, num_clusters) >= sk_begin(p, w + 1, num_clusters)) continue;
+                        const uint64_t *flag = p.flags + w * CS + pair_rank;
+                        const long long t0 = clock64();
+                        while (ptx::ld_acquire_gpu_u64(flag) != p.sk_stamp) {
+                            if (*abort_flag || clock64() - t0 > p.wait_limit) {
+                                *abort_flag = 1u;
+                                atomicCAS(p.error_word, 0u, kErrWaitPartial | (blockIdx.x << 8));
+                                break;
+                            }
+                        }
+                    }
+                }
+                ptx::named_barrier_sync(1, 32 * kWideEpiWarps);
+                if (live) {
+                    const uint32_t piece = (half * 4u + quarter) * 32u * uint32_t(Cfg::kHalfN) + lane * 4u;
+                    auto contributes = [&](uint32_t w) {
+                        return sk_begin(p, w, num_clusters) < sk_begin(p, w + 1, num_clusters);
+                    };
+                    // The owner's segment is this cluster's last: its main loop is done, so the operand
+                    // ring is idle.  Each 32-column piece of the first contributor's partial is one
+                    // contiguous 4 KB block; it is bulk-copied into one of two 4 KB buffers of this
+                    // warp in the ring, one piece ahead, and read from there (lane l, float4 j at
+                    // (j * 32 + l) * 16 bytes).  Other contributors, rare, are loaded in turn.
+                    uint32_t w0 = first_w;
+                    while (w0 < last_w && !contributes(w0)) ++w0;
+                    const bool have0 = w0 < last_w;
+                    const float *src0 = p.partials + size_t(w0 * CS + pair_rank) * kSlotFloats +
+                                        (half * 4u + quarter) * 32u * uint32_t(Cfg::kHalfN);
+                    const uint32_t land = base + Cfg::kOffA + (warp - 2u) * 8192u;
+                    const uint32_t bar_land = bar_drain + 8u * (1u + 2u * (warp - 2u));
+                    constexpr int kPieces = Cfg::kHalfN / 32;
+                    auto fetch = [&](int c) {  // lane 0: piece c into buffer c mod 2
+                        if (have0 && c < kPieces) {
+                            const uint32_t b = uint32_t(c) & 1u;
+                            ptx::mbar_arrive_expect_tx(bar_land + 8u * b, 4096u);
+                            ptx::bulk_load(land + 4096u * b, src0 + c * 1024, 4096u, bar_land + 8u * b);
+                        }
+                    };
+                    if (lane == 0) {
+                        ptx::fence_proxy_async_global();
+                        fetch(0);
+                        fetch(1);
+                    }
+                    int used = 0;  // pieces consumed, in order
+                    auto wait_piece = [&](int c) {
+                        const long long t0 = clock64();
+                        while (!ptx::mbar_try_wait(bar_land + 8u * (uint32_t(c) & 1u), (uint32_t(c) >> 1) & 1u)) {
+                            if (clock64() - t0 > p.wait_limit) {
+                                *abort_flag = 1u;
+                                atomicCAS(p.error_word, 0u, kErrWaitPartial | (blockIdx.x << 8));
+                                break;
+                            }
+                        }
+                    };
+                    // 32 columns at a time: load, add every contributor's partial, round to fp16
+                    auto chunk32 = [&](int c, uint32_t (&packed)[16]) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32_wait(t_col + uint32_t(32 * c), r);
+                        used = c + 1;
+                        if (have0) {
+                            const uint32_t b = uint32_t(c) & 1u;
+                            wait_piece(c);
+                            const uint32_t from = land + 4096u * b + lane * 16u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 v = ptx::ld_shared_f4(from + uint32_t(j) * 512u);
+                                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                            }
+                            // every lane has read the buffer: refill it with the piece after next
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) fetch(c + 2);
+                        }
+                        for (uint32_t w = w0 + 1; w < last_w; ++w) {
+                            if (!contributes(w)) continue;
+                            const float *src = p.partials + size_t(w * CS + pair_rank) * kSlotFloats + piece;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 v = ptx::ld_global_cg_f4(src + (c * 8 + j) * 128);
+                                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) packed[j] = pack_half2(r[2 * j], r[2 * j + 1]);
+                    };
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::kFullChunks; ++c) {
+                        const uint32_t col = col0 + uint32_t(64 * c);
+                        if (col >= p.n) break;
+                        uint32_t lo[16], hi[16];
+                        chunk32(2 * c, lo);
+                        chunk32(2 * c + 1, hi);
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            ptx::st_shared_v4(row_addr + ((uint32_t(j) ^ (lane & 7u)) << 4), lo[4 * j], lo[4 * j + 1],
+                                              lo[4 * j + 2], lo[4 * j + 3]);
+                            ptx::st_shared_v4(row_addr + ((uint32_t(j + 4) ^ (lane & 7u)) << 4), hi[4 * j],
+                                              hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&p.tmap_c, buf, int32_t(col), int32_t(row0));
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                    if constexpr (Cfg::kTail) {
+                        const uint32_t col = col0 + uint32_t(64 * Cfg::kFullChunks);
+                        if (col < p.n) {
+                            uint32_t w[16];
+                            chunk32(2 * Cfg::kFullChunks, w);
+                            if (lane == 0) ptx::bulk_wait_group_read<0>();
+                            __syncwarp();
+                            const uint32_t row32 = buf + lane * 64u;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                ptx::st_shared_v4(row32 + ((uint32_t(j) ^ ((lane >> 1) & 3u)) << 4), w[4 * j],
+                                                  w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_2d(&p.tmap_c32, buf, int32_t(col), int32_t(row0));
+                                ptx::bulk_commit_group();
+                            }
+                        }
+                    }
+                    // pieces fetched ahead but not consumed (columns past N): let them land before the
+                    // CTA can exit
+                    if (have0 && lane == 0)
+                        for (int c = used; c < used + 2 && c < kPieces; ++c) wait_piece(c);
+                }
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster_signal(ptx::map_to_rank(bar_acc_empty, 0u));
+                return true;
+            }
+        };
+        for_each_segment2<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
             const uint32_t row0 = mb * Cfg::kBM + pair_rank * 128u + quarter * 32u;
@@ -344,7 +552,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                 }
             }
             return true;
-        });
+        }, sk_segment);
         if (lane == 0) ptx::bulk_wait_group<0>();
     }
 

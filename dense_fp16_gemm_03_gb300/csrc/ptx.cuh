@@ -211,6 +211,22 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tm
         : "memory");
 }
 
+// Contiguous bulk copy global -> this CTA's shared memory of `bytes` (a
+// multiple of 16, both addresses 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses of global memory (e.g.
+// an acquire of a flag) before its later async-proxy accesses of it.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 2-D tiled store shared -> global (elements outside the tensor are skipped).
 __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y)
 {
@@ -439,6 +455,14 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v)
 {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -89,8 +89,8 @@ typedef struct gemm_f16_plan {
     int32_t cta_group;       /* 1: one CTA per MMA tile; 2: a CTA pair (cluster of 2) shares one */
     int32_t block_m;         /* output rows per cluster tile (128 * cta_group, times the CTA pairs a
                                 multicast cluster stacks along M) */
-    int32_t block_n;         /* output columns per cluster tile (wide tiles: 512 or 448, two MMAs of N = 256
-                                or 224; single CTAs sharing A by multicast: N times the CTAs along N) */
+    int32_t block_n;         /* output columns per cluster tile (wide tiles: 512, 448 or 320, two MMAs of N =
+                                256, 224 or 160; single CTAs sharing A by multicast: N times the CTAs along N) */
     int32_t block_k;         /* K depth of one pipeline stage (64) */
     int32_t stages;          /* shared-memory ring depth */
     int32_t raster_width;    /* N-columns per raster group (>= 1) */
@@ -118,16 +118,19 @@ typedef struct gemm_f16_plan {
  * wave.  A tile split between clusters is finished by the cluster holding
  * its first K block, which adds the fp32 partial tiles the others publish in
  * the workspace.  Workspace layout: grid partial tiles of 128 x (the
- * variant's MMA N) fp32 each, then grid 64-bit flags.  A flag is set to a
+ * variant's block_n, see gemm_f16_variant_info) fp32 each, then grid 64-bit
+ * flags.  A flag is set to a
  * stamp unique to the launch (a per-process random high word and a launch
  * counter), so flags left by earlier launches or found in fresh memory never
  * count and nothing needs clearing between launches; a workspace must not be
  * shared by launches that overlap on the GPU.  Every cluster of the grid
  * must be resident at once; the plan's
  * grid never exceeds that.  The fp32 partial sums change the rounding order
- * of split tiles only within the fp32 accumulation error.  The wide tiles
- * (256 x 512 and 256 x 448, block_n > 256) have no stream-K tail: asking for
- * one is GEMM_ERR_INVALID_ARG, and automatic plans never give them one.
+ * of split tiles only within the fp32 accumulation error.  For the wide tiles
+ * (256 x 512, 256 x 448 and 256 x 320, block_n > 256) a requested tail
+ * (stream_k = 1) covers only the partial last wave (every whole wave stays
+ * data-parallel; 512 KB partials per pair); automatic plans never give them
+ * one, because on GB300 it measured slower than the data-parallel waves.
  *
  * Split-K ("split_k == S > 1", stream_k 0): for products with fewer tiles
  * than resident clusters and a long K.  Each tile's K blocks are cut into S

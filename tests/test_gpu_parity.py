@@ -25,11 +25,9 @@ def _gpu():
     require_gpu()
 
 
-def _variants(stream_k=False):
-    """The compiled variants of this layout (B [N,K], fp16 C); with stream_k, those that have a
-    stream-K tail (tiles of at most 256 columns)."""
-    return [v for v in range(G.gemm_f16_variant_count()) if G.gemm_f16_variant_info(v)["layout"] == 0
-            and (not stream_k or G.gemm_f16_variant_info(v)["block_n"] <= 256)]
+def _variants():
+    """The compiled variants of this layout (B [N,K], fp16 C); every one of them has a stream-K tail."""
+    return [v for v in range(G.gemm_f16_variant_count()) if G.gemm_f16_variant_info(v)["layout"] == 0]
 
 
 # ------------------------------------------------------------------ small
@@ -100,7 +98,7 @@ SK_SHAPES = [(640, 1032, 520), (1000, 1000, 1000), (300, 520, 4096), (128, 256, 
 
 
 @pytest.mark.parametrize("shape", SK_SHAPES)
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15, 16, 17])
 def test_stream_k_exact(shape, variant):
     """Split tiles are summed from fp32 partials; on integer-valued operands
     every partial and every sum is exact, so the result is still bit-exact."""
@@ -121,11 +119,24 @@ def test_stream_k_tail_past_one_wave_exact(variant):
     assert_parity(run_gpu(A, B, variant=variant, stream_k=-1), A, B, exact=True)
 
 
+@pytest.mark.parametrize("variant", [15, 16, 17])
+def test_wide_tail_after_whole_waves_exact(variant):
+    """Wide tiles keep every whole wave data-parallel and split only the partial last wave over all
+    clusters: one whole wave plus a partial one (ragged edges, K in 40 blocks), bit for bit."""
+    M, N, K = 256 * 13, 5000, 2560
+    plan = G.gemm_f16_nt_plan_ex(M, N, K, variant, 0, 1)
+    slots = plan.grid // plan.cluster
+    assert plan.stream_k == 1 and plan.dp_tiles > 0 and plan.dp_tiles % slots == 0
+    assert 0 < plan.num_tiles - plan.dp_tiles < slots
+    A, B = inputs.make_operands(M, N, K, "eighths", seed=variant + 7)
+    assert_parity(run_gpu(A, B, variant=variant, stream_k=1), A, B, exact=True)
+
+
 @pytest.mark.parametrize("shape", [(777, 1000, 1536), (1024, 1024, 4096), (128, 2048, 16384)])
 def test_stream_k_tolerance(shape):
     M, N, K = shape
     A, B = inputs.make_operands(M, N, K, "normal", seed=M + K)
-    for v in _variants(stream_k=True):
+    for v in _variants():
         assert_parity(run_gpu(A, B, variant=v, stream_k=1), A, B)
 
 
@@ -136,7 +147,7 @@ def test_stream_k_reused_and_dirty_workspace(fill):
     M, N, K = 1000, 1000, 1000
     A, B = inputs.make_operands(M, N, K, "eighths", seed=fill + 1)
     A2, B2 = inputs.make_operands(M, N, K, "eighths", seed=fill + 2)
-    for v in (1, 2, 4):
+    for v in (1, 2, 4, 15):
         plan = G.gemm_f16_nt_plan_ex(M, N, K, v, 0, 1)
         assert plan.stream_k == 1
         ws = torch.full((int(plan.workspace_bytes),), fill, dtype=torch.uint8, device="cuda")
