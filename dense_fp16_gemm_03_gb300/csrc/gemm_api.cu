@@ -242,6 +242,22 @@ bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
     return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
+// The wide tiles (256 x 512, 256 x 448, 256 x 320) can take a stream-K tail
+// over the partial last wave only (every whole wave data-parallel), but the
+// automatic plans never give them one: measured on GB300 (burst, 400-launch
+// blocks) it lost everywhere -- 8192^3 575 against 565 us, 4096^3 85.3
+// against 79.7 us, 3000 x 5000 x 4096 78.4 against 68.6 us for the 448-column
+// tile -- even with the owner's partials bulk-copied into the idle ring.
+// With one accumulator filling tensor memory, about half the tail tiles are
+// cut three ways; the owner then waits for a middle contributor that ends
+// its whole range and publishes 256 KB per CTA through its ~95 GB/s port,
+// and adds one or two such partials, which costs more than the third of a
+// tile the tail saves.  A request for it (stream_k = 1) is honoured.
+bool wide_tail_pays(int64_t, int64_t, int64_t)
+{
+    return false;
+}
+
 // Clusters that share a stream-K tail of `tiles` tiles when no whole wave is
 // left to run data-parallel.  A tile split over w clusters is finished by its
 // owner adding the other w - 1 partials one after another (~2,800 cycles each
@@ -308,6 +324,11 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
         return s < 1 ? 1 : s;
     };
     if (m <= 128) return 2 * cdiv(n, 256) >= slots_of(13) ? 13 : 1;
+    // Small products whose 128 x 128 tiles fit one wave of single CTAs and whose K is too short to be
+    // split (fewer than 8 K blocks): the launch is latency-bound, and single CTAs halve each one's
+    // main loop and its share of C to store (256^3: 4.34 us per launch against 6.42 for the
+    // 256 x 256 pair tile, 5.00 for 128 x 256 and 5.80 for 256 x 128, back to back on GB300).
+    if (k_blocks < 8 && cdiv(m, 128) * cdiv(n, 128) <= int64_t(num_sms)) return 1;
     if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
     const int64_t pair_tiles_m = cdiv(m, 256), tiles_n = cdiv(n, 256);
     int32_t alt = 2;
@@ -434,27 +455,33 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     p.dp_tiles = p.num_tiles;
     p.sk_iters = 0;
     p.workspace_bytes = 0;
-    // the wide variants have no stream-K tail: asking for one is an error, the automatic choice skips it
-    const bool sk_capable = !is_wide(var);
-    if (stream_k == 1 && !sk_capable) return GEMM_ERR_INVALID_ARG;
-    // rotation or a stream-K tail (tail_choice); with the tail forbidden or unavailable, rotation alone
+    // rotation or a stream-K tail (tail_choice; the wide tiles' own rule, wide_tail_pays); with the tail
+    // forbidden, rotation alone
+    const bool wide = is_wide(var);
     bool rotate = false, tail = false;
     tail_choice(p.tiles_m, p.tiles_n, p.k_blocks, slots, &rotate, &tail);
-    if (stream_k == 0 || !sk_capable) rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks);
+    if (wide) {
+        tail = wide_tail_pays(p.num_tiles, p.k_blocks, slots);
+        rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks) && !tail;
+    }
+    if (stream_k == 0) rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks);
     if (stream_k == 1) rotate = false;
     p.k_rotate = rotate ? 1 : 0;
-    const bool want_sk = stream_k == 1 || (stream_k < 0 && sk_capable && tail);
+    const bool want_sk = stream_k == 1 || (stream_k < 0 && tail);
     if (want_sk && p.num_tiles > 0) {
-        // whole waves but the last one or two stay data-parallel; the rest is split evenly
+        // whole waves but the last one or two stay data-parallel; the rest is split evenly.  For the
+        // wide tiles every whole wave stays data-parallel (a 256 x 512 fp32 partial is 512 KB, so only
+        // the partial last wave is worth splitting)
         const int64_t full_waves = p.num_tiles / slots;
-        const int64_t dp = full_waves >= 1 ? (full_waves - 1) * slots : 0;
+        int64_t dp = full_waves >= 1 ? (full_waves - 1) * slots : 0;
+        if (wide) dp = full_waves * slots;
         const int64_t sk_iters = (p.num_tiles - dp) * p.k_blocks;
         const int64_t workers = dp == 0 ? tail_workers(p.num_tiles, p.k_blocks, slots) : slots;
         // the tail must shorten the longest cluster's work: data-parallel, the tail's tiles take
         // ceil(left / min(left, slots)) tiles on some cluster; the tail gives each left / workers
         const int64_t left = p.num_tiles - dp;
-        const int64_t dp_waves = cdiv(left, left < slots ? left : slots);
-        if (sk_iters >= workers && left < dp_waves * workers) {
+        const int64_t dp_waves = left > 0 ? cdiv(left, left < slots ? left : slots) : 0;
+        if (left > 0 && sk_iters >= workers && left < dp_waves * workers) {
             clusters = workers;
             p.stream_k = 1;
             p.dp_tiles = dp;
@@ -542,7 +569,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
             return GEMM_ERR_INVALID_ARG;
     } else {
         // owners wait for contributors: every cluster must be resident at once
-        if (plan.stream_k != 1 || is_wide(kVariants[plan.variant]) || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
+        if (plan.stream_k != 1 || plan.dp_tiles < 0 || plan.dp_tiles > plan.num_tiles ||
             plan.sk_iters != (plan.num_tiles - plan.dp_tiles) * plan.k_blocks || plan.sk_iters < workers ||
             workers > dev->max_clusters[plan.variant] ||
             int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, kVariants[plan.variant].bn))

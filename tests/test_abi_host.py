@@ -166,7 +166,7 @@ def test_no_cuda_device_is_an_error_not_a_crash(L):
 
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (8192, 8192, 8192),
                                    (1000, 1000, 1000), (128, 256, 8192)])
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15, 16, 17])
 def test_stream_k_plan_invariants(L, shape, variant):
     m, n, k = shape
     for sms in (148, 152):
@@ -176,6 +176,8 @@ def test_stream_k_plan_invariants(L, shape, variant):
             assert p.sk_iters == (p.num_tiles - p.dp_tiles) * p.k_blocks
             assert p.sk_iters >= workers and p.dp_tiles % workers == 0
             assert p.num_tiles - p.dp_tiles <= 2 * workers            # at most two waves are split
+            if G.gemm_f16_variant_info(variant)["block_n"] > 256:     # wide tiles: only a partial last wave
+                assert p.num_tiles - p.dp_tiles < workers
             bn = G.gemm_f16_variant_info(variant)["block_n"]        # one CTA's partial tile is 128 x bn
             assert p.workspace_bytes >= p.grid * 128 * bn * 4 + p.grid * 8
             slots = sms // p.cluster
@@ -228,7 +230,7 @@ def test_gb300_plans_of_the_configured_workloads(L):
     lines), and the committed DRAM-traffic captures were taken on exactly those plans."""
     import json
     expect = {
-        "square_256": (2, 0, 0, 0),
+        "square_256": (1, 0, 0, 0),
         "square_4096": (15, 0, 0, 0),
         "square_8192": (15, 0, 0, 0),
         "ragged_3000x5000x4096": (16, 0, 0, 0),
@@ -291,8 +293,6 @@ def _segments(p):
 def test_stream_k_covers_every_k_block_once(L, shape):
     m, n, k = shape
     for variant in range(G.gemm_f16_variant_count()):
-        if G.gemm_f16_variant_info(variant)["block_n"] > 256:
-            continue                                                  # no stream-K tail on the wide tile
         p = G.gemm_f16_nt_plan_for(m, n, k, 152, 0, variant, 0, 1)
         if not p.stream_k:
             continue
@@ -343,7 +343,9 @@ def test_k_rotation_rule(L):
     ((3000, 5000, 4096), 4, 1, False),     # with 38 clusters of four, multicast pairs and a stream-K tail
                                            # (3.3 waves) edge out 144 tiles of 256 x 448 (95% of 2 waves);
                                            # GB300 fits 36, and there the 256 x 448 tile wins
-    ((256, 256, 256), 2, 0, False),        # one tile: the wide tile would compute twice the area
+    ((256, 256, 256), 1, 0, False),        # latency-bound: four single-CTA 128 x 128 tiles (4.34 us against 6.42
+                                           # for one 256 x 256 pair tile)
+    ((256, 256, 512), 2, 0, False),        # eight K blocks: the pair tile as before
     ((128, 16384, 16384), 13, 0, False),   # M <= 128, B rows for 64 of 76 pairs: swapped pair tiles, rotated
     ((100, 20000, 8192), 13, 1, False),    # 79 pair tiles for 76 pairs: a stream-K tail, not a second wave
     ((128, 8192, 8192), 1, 0, True),       # 32 pair tiles would idle most pairs: 128 x 128 tiles, K split
