@@ -389,16 +389,42 @@ def time_workload(G, w, dev, stream, sampler, launches, warmup, peaks):
     if st != G.GEMM_OK:
         raise RuntimeError("%s: kernel reported error word 0x%x" % (w.name, code))
     ms = e0.elapsed_time(e1) / launches
+    # The same launches replayed from a CUDA graph: device time without the per-call host work (the
+    # Python binding and the library's planning and tensor-map encoding), which bounds the small,
+    # latency-bound products when they are launched one call at a time.
+    ms_graph = None
+    try:
+        n_graph = min(launches, 400)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n_graph):
+                a, b, c = bufs[i % sets]
+                G.gemm_f16_nt_ws(a, b, c, ws, stream=stream)
+        with torch.cuda.stream(stream):  # a graph replays on the current stream
+            graph.replay()
+            stream.synchronize()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            graph.replay()
+            g1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_graph = g0.elapsed_time(g1) / n_graph
+        del graph
+    except RuntimeError:
+        ms_graph = None
     mhz = [float(s[2]) for (t, s) in list(sampler.samples) if len(s) > 2 and t0 - 0.05 <= t <= t1 + 0.15
            and s[2].replace(".", "", 1).isdigit()]
     reasons = sorted({n for (t, s) in list(sampler.samples) if t0 - 0.05 <= t <= t1 + 0.15
                       for i, n in enumerate(ClockSampler.REASONS) if len(s) > 6 + i and s[6 + i].lower() == "active"})
-    regime = timing_regime(ms * launches, {"reasons": reasons})
+    # each product is timed alone for a short region (milliseconds): the burst denominator, whatever
+    # throttle state the samples around it caught from the work before
+    regime = timing_regime(ms * launches, None)
     tflops = w.flops / (ms * 1e-3) / 1e12
     entry = {
         "M": w.M, "N": w.N, "K": w.K, "distribution": w.dist, "seed": w.seed,
         "ms": ms, "tflops": tflops, "launches": launches, "operand_copies": sets,
         "host_us_per_call": host_s / launches * 1e6,
+        "ms_graph": ms_graph, "tflops_graph": (w.flops / (ms_graph * 1e-3) / 1e12) if ms_graph else None,
         "sm_mhz": statistics.median(mhz) if mhz else None, "clock_reasons": reasons,
         "plan": {k: getattr(plan, k) for k in ("variant", "block_m", "block_n", "grid", "stream_k", "split_k",
                                                "k_rotate", "raster_width")},
@@ -427,6 +453,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="square_8192", choices=sorted(inputs.BY_NAME))
+    ap.add_argument("--shape", default=None, help="MxNxK: time this product instead of a configured workload "
+                    "(uniform operands, seed 0; for measurement and profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip timing the other configured products")
@@ -443,6 +471,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = inputs.BY_NAME[args.workload]
+    if args.shape:
+        m_, n_, k_ = (int(x) for x in args.shape.lower().split("x"))
+        w = inputs.Workload("shape_%dx%dx%d" % (m_, n_, k_), m_, n_, k_, "uniform", 0)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, w, world, rank)
