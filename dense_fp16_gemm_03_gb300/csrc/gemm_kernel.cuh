@@ -413,9 +413,51 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+
+    // Where this CTA's boxes of a segment start: the A rows m0, the B rows (or, B stored [K, N], the
+    // columns) n0, and the K-walk rotation.  With k_rotate, a whole tile walks its K blocks from a
+    // per-tile offset, wrapping around: when no operand strip is shared between tiles, lockstep K
+    // walks make every CTA read the same K column of rows a power-of-two pitch apart, which piles the
+    // requests onto the same DRAM channels.  The MMA consumes stages in order either way.
+    auto segment_origin = [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi, int32_t &m0, int32_t &n0, uint32_t &rot) {
+        uint32_t mb, nb;
+        raster_coord(p.raster, tile, mb, nb);
+        m0 = Cfg::kAMC ? int32_t(mb * 128u + cta_rank * Cfg::kASlice)
+                       : int32_t(mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u);
+        n0 = Cfg::kAMC ? int32_t((nb * MC + cta_rank) * BN)
+                       : int32_t(nb * BN + pair_rank * Cfg::kBNCta + pair * Cfg::kBSlice);
+        const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
+        rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
+    };
+
     // Launched as a programmatic dependent: the set-up above overlaps the tail of the previous
-    // kernel in the stream; no global memory is touched before that kernel has completed.
+    // kernel in the stream, and nothing is read or written through the generic or the TMA load path
+    // before that kernel has completed (griddepcontrol.wait).  Before the wait, the producer only asks
+    // L2 to prefetch the boxes of its first ring fills: a prefetch is a hint with no effect on
+    // results (L2 is where every write lands, so a line the previous kernel writes afterwards is
+    // still read as written), and it lets this launch's first reads from DRAM overlap the previous
+    // launch's last tiles.
     ptx::griddep_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
+            int32_t m0, n0;
+            uint32_t rot;
+            segment_origin(tile, k_lo, k_hi, m0, n0, rot);
+            for (uint32_t kb = k_lo; kb < k_hi && kb < k_lo + uint32_t(STAGES); ++kb) {
+                uint32_t kr = kb + rot;
+                if (kr >= p.k_blocks) kr -= p.k_blocks;
+                const int32_t k0 = int32_t(kr * kBlockK);
+                ptx::tma_prefetch_2d(&p.tmap_a, k0, m0);
+                if constexpr (B_KMAJOR) {
+                    ptx::tma_prefetch_2d(&p.tmap_b, k0, n0);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < Cfg::kBNCta / 64; ++h) ptx::tma_prefetch_2d(&p.tmap_b, n0 + 64 * h, k0);
+                }
+            }
+            return false;  // the first segment only
+        });
+    }
     ptx::griddep_wait();
 
     if (warp == 0) {
@@ -424,18 +466,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             uint32_t stage = 0, phase = 0, fills = 0;
             bool ok = true;
             for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
-                uint32_t mb, nb;
-                raster_coord(p.raster, tile, mb, nb);
-                const int32_t m0 = Cfg::kAMC ? int32_t(mb * 128u + cta_rank * Cfg::kASlice)
-                                             : int32_t(mb * Cfg::kBMCluster + pair * Cfg::kBM + pair_rank * 128u);
-                const int32_t n0 = Cfg::kAMC ? int32_t((nb * MC + cta_rank) * BN)
-                                             : int32_t(nb * BN + pair_rank * Cfg::kBNCta + pair * Cfg::kBSlice);
-                // With k_rotate, a whole tile walks its K blocks from a per-tile offset, wrapping
-                // around: when no operand strip is shared between tiles, lockstep K walks make every
-                // CTA read the same K column of rows a power-of-two pitch apart, which piles the
-                // requests onto the same DRAM channels.  The MMA consumes stages in order either way.
-                const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
-                const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
+                int32_t m0, n0;
+                uint32_t rot;
+                segment_origin(tile, k_lo, k_hi, m0, n0, rot);
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb, ++fills) {
                     if (!wait_bounded<CS>(bar_empty(stage), phase ^ 1u, p, abort_flag, kErrWaitEmpty)) {
                         ok = false;

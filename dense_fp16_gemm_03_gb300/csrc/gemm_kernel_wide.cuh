@@ -161,7 +161,28 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
     ptx::cluster_sync();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // As in gemm_kernel.cuh: before waiting for the previous kernel, only L2 prefetches of the first
+    // ring fills' boxes (hints, no effect on results).
     ptx::griddep_launch_dependents();
+    if (warp == 0 && lane == 0) {
+        for_each_segment<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
+            uint32_t mb, nb;
+            raster_coord(p.raster, tile, mb, nb);
+            const int32_t m0 = int32_t(mb * Cfg::kBM + pair_rank * 128u);
+            const int32_t n0 = int32_t(nb * Cfg::kBN + pair_rank * uint32_t(Cfg::kBBoxRows));
+            const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
+            const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
+            for (uint32_t kb = k_lo; kb < k_hi && kb < k_lo + uint32_t(STAGES); ++kb) {
+                uint32_t kr = kb + rot;
+                if (kr >= p.k_blocks) kr -= p.k_blocks;
+                const int32_t k0 = int32_t(kr * kBlockK);
+                ptx::tma_prefetch_2d(&p.tmap_a, k0, m0);
+                ptx::tma_prefetch_2d(&p.tmap_b, k0, n0);
+                ptx::tma_prefetch_2d(&p.tmap_b, k0, n0 + Cfg::kHalfN);
+            }
+            return false;  // the first segment only
+        });
+    }
     ptx::griddep_wait();
 
     if (warp == 0) {

@@ -227,6 +227,15 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Prefetch the box at {x, y} of a 2-D tensor map into L2 (no shared-memory
+// destination, no completion; a hint with no effect on results).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled store shared -> global (elements outside the tensor are skipped).
 __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y)
 {
