@@ -302,6 +302,26 @@ __device__ __forceinline__ void for_each_segment2(const KernelParams &p, uint32_
     }
 }
 
+// As for_each_segment2, with this cluster's last data-parallel tile handed to
+// f_last instead of f_dp when no stream-K segment follows it (then nothing
+// of this cluster uses the operand ring or tensor memory after that tile).
+// The last tile is peeled off the loop, so the three functions' bodies do
+// not share live ranges.
+template <bool kSplitK = true, class FD, class FL, class FS>
+__device__ __forceinline__ void for_each_segment3(const KernelParams &p, uint32_t worker, uint32_t workers, FD &&f_dp,
+                                                  FL &&f_last, FS &&f_sk)
+{
+    if ((kSplitK && p.split_k > 1) || p.sk_iters != 0) {
+        for_each_segment2<kSplitK>(p, worker, workers, f_dp, f_sk);
+        return;
+    }
+    if (worker >= p.dp_tiles) return;
+    const uint32_t last = worker + (p.dp_tiles - 1u - worker) / workers * workers;
+    for (uint32_t tile = worker; tile < last; tile += workers)
+        if (!f_dp(tile, 0u, p.k_blocks)) return;
+    f_last(last, 0u, p.k_blocks);
+}
+
 // The same walk with one function for every segment.
 template <bool kSplitK = true, class F>
 __device__ __forceinline__ void for_each_segment(const KernelParams &p, uint32_t worker, uint32_t workers, F &&f)

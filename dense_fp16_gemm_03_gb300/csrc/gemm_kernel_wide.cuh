@@ -44,6 +44,14 @@ namespace gemm_f16 {
 constexpr int kWideEpiWarps = 8;
 constexpr int kWideThreads = 64 + 32 * kWideEpiWarps;
 
+// Shared memory one epilogue warp stages its whole 32 x HALF_N piece in, on a cluster's last tile:
+// one 4 KB box per 64-column chunk (and one for a 32-column tail).
+template <int HALF_N>
+__host__ __device__ constexpr int wide_final_bytes()
+{
+    return ((HALF_N + 63) / 64) * 4096;
+}
+
 template <int STAGES, int HALF_N>
 struct WideCfg {
     static_assert(HALF_N % 32 == 0 && HALF_N >= 128 && HALF_N <= 256, "one MMA's N: whole 32-column chunks");
@@ -73,6 +81,8 @@ struct WideCfg {
     static constexpr int kTmemCols = 512;
     static_assert(kBSubBytes % 1024 == 0, "B sub-tiles stay 1024-byte aligned for the 128-byte swizzle");
     static_assert(STAGES * (kABytes + kBBytes) >= kWideEpiWarps * 2 * 4096, "partial pieces land in the idle ring");
+    static_assert(STAGES * (kABytes + kBBytes) >= kWideEpiWarps * wide_final_bytes<HALF_N>(),
+                  "the last tile's pieces are staged in the idle ring");
     static_assert(kHalfCol + kHalfN <= kTmemCols, "both accumulator halves fit tensor memory");
     static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
 };
@@ -277,6 +287,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
         const uint32_t row_addr = buf + lane * 128u;
         const uint32_t t_col = tmem_base + ((quarter * 32u) << 16) + half * uint32_t(Cfg::kHalfCol);
         constexpr int kHeld = Cfg::kFullChunks - 1;
+        constexpr int kFinalBytes = wide_final_bytes<HALF_N>();
         // Stream-K partial tile of one CTA in the workspace: 128 rows x kBN fp32.  Warp piece
         // (half, quarter) = 32 rows x HALF_N columns at (half * 4 + quarter) * 32 * HALF_N; inside it,
         // 32-column chunk c, float4 j (columns 32c + 4j ..) of lane l at ((c * 8 + j) * 32 + l) * 4,
@@ -478,7 +489,66 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                 return true;
             }
         };
-        for_each_segment2<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
+        // this cluster's last tile (no stream-K segment after it): its MMAs consumed every ring stage
+        // and no load follows, so the ring is idle.  Each warp stages its whole piece there (one 4 KB box
+        // per 64-column chunk, 128-byte swizzled, then the 32-column tail box) and issues all its
+        // stores at once instead of one at a time through its staging buffer.
+        auto last_tile = [&](uint32_t tile, uint32_t, uint32_t) {
+            uint32_t mb, nb;
+            raster_coord(p.raster, tile, mb, nb);
+            const uint32_t row0 = mb * Cfg::kBM + pair_rank * 128u + quarter * 32u;
+            const uint32_t col0 = nb * Cfg::kBN + half * uint32_t(Cfg::kHalfN);
+            const bool ok = wait_bounded<CS>(bar_acc_full, acc_phase, p, abort_flag, kErrWaitAccFull);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            acc_phase ^= 1u;
+            ptx::tc_fence_after_sync();
+            const bool live = (row0 < p.m) && (col0 < p.n);
+            if (live) {
+                const uint32_t area = base + Cfg::kOffA + (warp - 2u) * uint32_t(kFinalBytes);
+#pragma unroll 1
+                for (int c = 0; c < Cfg::kFullChunks; ++c) {
+                    const uint32_t col = col0 + uint32_t(64 * c);
+                    if (col >= p.n) break;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32_wait(t_col + uint32_t(64 * c + 32 * s), r);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w[16 * s + j] = pack_half2(r[2 * j], r[2 * j + 1]);
+                    }
+                    const uint32_t box = area + uint32_t(c) * uint32_t(kStoreBufBytes);
+                    stage_row_sw128(box + lane * 128u, lane, w);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::tma_store_2d(&p.tmap_c, box, int32_t(col), int32_t(row0));
+                }
+                if constexpr (Cfg::kTail) {
+                    const uint32_t col = col0 + uint32_t(64 * Cfg::kFullChunks);
+                    if (col < p.n) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32_wait(t_col + uint32_t(64 * Cfg::kFullChunks), r);
+                        const uint32_t box = area + uint32_t(Cfg::kFullChunks) * uint32_t(kStoreBufBytes);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            ptx::st_shared_v4(box + lane * 64u + ((uint32_t(j) ^ ((lane >> 1) & 3u)) << 4),
+                                              pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                                              pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                                              pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                                              pack_half2(r[8 * j + 6], r[8 * j + 7]));
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) ptx::tma_store_2d(&p.tmap_c32, box, int32_t(col), int32_t(row0));
+                    }
+                }
+                if (lane == 0) ptx::bulk_commit_group();
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster_signal(ptx::map_to_rank(bar_acc_empty, 0u));
+            return true;
+        };
+        for_each_segment3<false>(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t, uint32_t) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
             const uint32_t row0 = mb * Cfg::kBM + pair_rank * 128u + quarter * 32u;
@@ -573,7 +643,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                 }
             }
             return true;
-        }, sk_segment);
+        }, last_tile, sk_segment);
         if (lane == 0) ptx::bulk_wait_group<0>();
     }
 
