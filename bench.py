@@ -433,7 +433,11 @@ def time_workload(G, w, dev, stream, sampler, launches, warmup, peaks):
         "algorithmic_gbs": w.algorithmic_bytes / (ms * 1e-3) / 1e9,
     }
     hbm = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
-    if w.flops / w.algorithmic_bytes < (entry["roofline"]["peak"] * 1e12) / (hbm * 1e9):
+    if w.flops < 1e9:
+        # a few tiles on a few SMs: launch and pipeline latency bound it, not a roofline
+        entry["roofline"] = {"bound": "latency", "achieved": tflops, "unit": UNIT, "peak": None, "frac": None,
+                             "regime": regime, "tensor": entry["roofline"]}
+    elif w.flops / w.algorithmic_bytes < (entry["roofline"]["peak"] * 1e12) / (hbm * 1e9):
         # below the ridge point: HBM bounds the product
         entry["roofline"] = {
             "bound": "hbm", "achieved": entry["algorithmic_gbs"], "peak": hbm, "unit": "GB/s",

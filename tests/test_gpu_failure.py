@@ -21,7 +21,7 @@ def _gpu():
     require_gpu()
 
 
-@pytest.mark.parametrize("variant", [0, 2, 4, 11, 13, 15, 16])
+@pytest.mark.parametrize("variant", [0, 2, 4, 11, 13, 15, 16, 17])
 def test_starved_wait_reports_timeout_and_recovers(variant):
     """The skipped fill starves the first CTA's MMA (or, for the clusters that share a tile by
     multicast, every MMA that waits for that CTA's slice).  Before the CTAs exit, the owners of the
