@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
             const int32_t m0 = int32_t(mb * Cfg::kBM + pair_rank * 128u);
             const int32_t n0 = int32_t(nb * Cfg::kBN + pair_rank * uint32_t(Cfg::kBBoxRows));
             const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
-            const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
+            const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * kRotateStride) % p.k_blocks) : 0u;
             for (uint32_t kb = k_lo; kb < k_hi && kb < k_lo + uint32_t(STAGES); ++kb) {
                 uint32_t kr = kb + rot;
                 if (kr >= p.k_blocks) kr -= p.k_blocks;
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) gemm_f16_nt_wide_kernel(const
                 // half of MMA h
                 const int32_t n0 = int32_t(nb * Cfg::kBN + pair_rank * uint32_t(Cfg::kBBoxRows));
                 const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
-                const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * 37u) % p.k_blocks) : 0u;
+                const uint32_t rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * kRotateStride) % p.k_blocks) : 0u;
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb, ++fills) {
                     if (!wait_bounded<CS>(bar_empty(stage), phase ^ 1u, p, abort_flag, kErrWaitEmpty)) {
                         ok = false;
