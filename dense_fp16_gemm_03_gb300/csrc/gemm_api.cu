@@ -519,6 +519,11 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     return GEMM_OK;
 }
 
+// Launch a plan this library made for the current device (device_plan) or one run_plan has
+// validated: the workspace the caller passed is checked, the plan itself is not checked again.
+gemm_status_t launch_plan(const gemm_f16_plan_t &plan, const DeviceInfo *dev, const void *a, const void *b, void *c,
+                          void *ws, size_t ws_bytes, cudaStream_t stream, uint32_t skip_fill, long long wait_limit);
+
 gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b, void *c, void *ws,
                        size_t ws_bytes, cudaStream_t stream, uint32_t skip_fill, long long wait_limit)
 {
@@ -532,14 +537,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
     if (plan.variant < 0 || plan.variant >= kNumVariants) return GEMM_ERR_INVALID_ARG;
-    const size_t c_elem = kVariants[plan.variant].layout == 1 ? 4u : 2u;
-    if (plan.k == 0) {
-        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * c_elem, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-        return GEMM_OK;
-    }
+    if (plan.k == 0) return launch_plan(plan, dev, a, b, c, ws, ws_bytes, stream, skip_fill, wait_limit);
     // the plan must be consistent with what this library computes for its shape
     gemm_f16_plan_t check;
     st = make_plan(plan.m, plan.n, plan.k, plan.num_sms, 0, plan.variant, plan.raster_width, 0, &check);
@@ -574,9 +572,28 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
             workers > dev->max_clusters[plan.variant] ||
             int64_t(plan.workspace_bytes) != streamk_workspace_bytes(plan.grid, kVariants[plan.variant].bn))
             return GEMM_ERR_INVALID_ARG;
+    }
+    return launch_plan(plan, dev, a, b, c, ws, ws_bytes, stream, skip_fill, wait_limit);
+}
+
+gemm_status_t launch_plan(const gemm_f16_plan_t &plan, const DeviceInfo *dev, const void *a, const void *b, void *c,
+                          void *ws, size_t ws_bytes, cudaStream_t stream, uint32_t skip_fill, long long wait_limit)
+{
+    if (plan.m == 0 || plan.n == 0) return GEMM_OK;
+    if (plan.workspace_bytes > 0) {
+        if (ws == nullptr || ws_bytes < plan.workspace_bytes) return GEMM_ERR_WORKSPACE;
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
     }
     const Variant &var = kVariants[plan.variant];
+    if (plan.k == 0) {
+        const size_t c_elem = var.layout == 1 ? 4u : 2u;
+        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * c_elem, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
+    gemm_status_t st = GEMM_OK;
     if (var.mc > 1) {
         // Cluster multicast loads deliver one copy of a tile to several CTAs of this GPU; they are
         // only used on this GPU's own device memory (never on a peer's or on host-mapped memory).
@@ -705,7 +722,7 @@ namespace {
 
 // Plan for the current device; arguments as in gemm_f16_nt_plan_for.
 gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int32_t raster_width, int32_t stream_k,
-                          gemm_f16_plan_t *out, int32_t layout = 0)
+                          gemm_f16_plan_t *out, int32_t layout = 0, DeviceInfo **dev_out = nullptr)
 {
     if (!out) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_shape(m, n, k);
@@ -714,6 +731,7 @@ gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int3
     DeviceInfo *dev = nullptr;
     st = device_info(&dev);
     if (st != GEMM_OK) return st;
+    if (dev_out) *dev_out = dev;
     return make_plan(m, n, k, dev->num_sms, 0, variant, raster_width, stream_k, out, dev->max_clusters, layout);
 }
 
@@ -836,10 +854,11 @@ gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, con
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
     gemm_f16_plan_t p;
-    st = device_plan(m, n, k, -1, 0, -1, &p);
+    DeviceInfo *dev = nullptr;
+    st = device_plan(m, n, k, -1, 0, -1, &p, 0, &dev);
     if (st != GEMM_OK) return st;
-    return run_plan(p, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
-                    default_wait_limit(p.k_blocks));
+    return launch_plan(p, dev, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                       default_wait_limit(p.k_blocks));
 }
 
 gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *c,
@@ -851,10 +870,11 @@ gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const 
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
     gemm_f16_plan_t p;
-    st = device_plan(m, n, k, -1, 0, 0, &p);
+    DeviceInfo *dev = nullptr;
+    st = device_plan(m, n, k, -1, 0, 0, &p, 0, &dev);
     if (st != GEMM_OK) return st;
-    return run_plan(p, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream), ~0u,
-                    default_wait_limit(p.k_blocks));
+    return launch_plan(p, dev, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                       default_wait_limit(p.k_blocks));
 }
 
 gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c, void *workspace,
@@ -880,10 +900,11 @@ gemm_status_t gemm_f16_nn_f32_ws(int64_t m, int64_t n, int64_t k, const void *a,
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
     gemm_f16_plan_t p;
-    st = device_plan(m, n, k, -1, 0, workspace ? -1 : 0, &p, 1);
+    DeviceInfo *dev = nullptr;
+    st = device_plan(m, n, k, -1, 0, workspace ? -1 : 0, &p, 1, &dev);
     if (st != GEMM_OK) return st;
-    return run_plan(p, a, b, d, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
-                    default_wait_limit(p.k_blocks));
+    return launch_plan(p, dev, a, b, d, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                       default_wait_limit(p.k_blocks));
 }
 
 gemm_status_t gemm_f16_nn_f32(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *d,
@@ -1088,7 +1109,8 @@ extern "C" gemm_status_t gemm_f16_nt_noalloc(int64_t m, int64_t n, int64_t k, co
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
     gemm_f16_plan_t p;
-    st = device_plan(m, n, k, -1, 0, -1, &p);
+    DeviceInfo *dev = nullptr;
+    st = device_plan(m, n, k, -1, 0, -1, &p, 0, &dev);
     if (st != GEMM_OK) return st;
     if (p.workspace_bytes > uint64_t(GEMM_F16_STATIC_SCRATCH_BYTES)) return GEMM_ERR_WORKSPACE;
     void *scratch = nullptr;
@@ -1096,6 +1118,6 @@ extern "C" gemm_status_t gemm_f16_nt_noalloc(int64_t m, int64_t n, int64_t k, co
         st = noalloc_scratch(&scratch);
         if (st != GEMM_OK) return st;
     }
-    return run_plan(p, a, b, c, scratch, size_t(GEMM_F16_STATIC_SCRATCH_BYTES), reinterpret_cast<cudaStream_t>(stream),
-                    ~0u, default_wait_limit(p.k_blocks));
+    return launch_plan(p, dev, a, b, c, scratch, size_t(GEMM_F16_STATIC_SCRATCH_BYTES),
+                       reinterpret_cast<cudaStream_t>(stream), ~0u, default_wait_limit(p.k_blocks));
 }

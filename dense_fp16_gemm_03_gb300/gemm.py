@@ -135,6 +135,18 @@ def _check(status, where):
         raise GemmError(status, where)
 
 
+_torch = None
+
+
+def _tm():
+    """torch, imported once (the binding works without it for plain integer addresses)."""
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
+
+
 def _ptr(x):
     if x is None:
         return None
@@ -145,8 +157,7 @@ def _ptr(x):
 
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _tm().cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -216,36 +227,56 @@ def gemm_f16_nt_workspace_size(m, n, k):
 # ------------------------------------------------------------------ launches
 
 def _shape(a, b):
-    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
+    sa, sb = a.shape, b.shape
+    if len(sa) != 2 or len(sb) != 2 or sa[1] != sb[1]:
         raise ValueError("a must be [M,K] and b [N,K]")
-    import torch
-    for t in (a, b):
-        if t.dtype != torch.float16 or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError("operands must be contiguous float16 CUDA tensors")
-    return a.shape[0], b.shape[0], a.shape[1]
+    f16 = _tm().float16
+    if (a.dtype is not f16 or b.dtype is not f16 or not (a.is_cuda and b.is_cuda)
+            or not (a.is_contiguous() and b.is_contiguous())):
+        raise ValueError("operands must be contiguous float16 CUDA tensors")
+    return sa[0], sb[0], sa[1]
+
+
+def _check_matrix(t, rows, cols, dtype_name, what):
+    """A device buffer given as a tensor must be a contiguous CUDA matrix of the expected shape and
+    dtype (the C ABI sees only its address).  Raw integer addresses are the caller's responsibility."""
+    if t is None or isinstance(t, int):
+        return
+    if (t.shape != (rows, cols) or t.dtype is not getattr(_tm(), dtype_name) or not t.is_cuda
+            or not t.is_contiguous()):
+        raise ValueError("%s must be a contiguous %s CUDA tensor of shape [%d, %d]" % (what, dtype_name, rows, cols))
 
 
 def gemm_f16_nt(a, b, c=None, stream=None):
     """C = A . B^T for contiguous fp16 CUDA tensors A [M,K], B [N,K]; returns C [M,N]."""
-    import torch
     m, n, k = _shape(a, b)
     if c is None:
+        torch = _tm()
         c = torch.empty((m, n), dtype=torch.float16, device=a.device)
-    elif tuple(c.shape) != (m, n) or c.dtype != torch.float16 or not c.is_contiguous():
-        raise ValueError("c must be a contiguous float16 [M,N] tensor")
+    else:
+        _check_matrix(c, m, n, "float16", "c")
     _check(lib().gemm_f16_nt(m, n, k, _ptr(a), _ptr(b), _ptr(c), _stream(stream)), "gemm_f16_nt")
     return c
 
 
 def gemm_f16_nt_ws(a, b, c, workspace, stream=None):
     m, n, k = _shape(a, b)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check_matrix(c, m, n, "float16", "c")
+    ws_bytes = 0 if workspace is None else workspace.nbytes
     _check(lib().gemm_f16_nt_ws(m, n, k, _ptr(a), _ptr(b), _ptr(c), _ptr(workspace), ws_bytes,
                                 _stream(stream)), "gemm_f16_nt_ws")
     return c
 
 
 def gemm_f16_nt_run(plan, a, b, c, workspace=None, stream=None):
+    m, n, k = int(plan.m), int(plan.n), int(plan.k)
+    _check_matrix(a, m, k, "float16", "a")
+    if plan.layout == 0:
+        _check_matrix(b, n, k, "float16", "b")
+        _check_matrix(c, m, n, "float16", "c")
+    else:
+        _check_matrix(b, k, n, "float16", "b")
+        _check_matrix(c, m, n, "float32", "d")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().gemm_f16_nt_run(ctypes.byref(plan), _ptr(a), _ptr(b), _ptr(c), _ptr(workspace), ws_bytes,
                                  _stream(stream)), "gemm_f16_nt_run")
@@ -260,8 +291,9 @@ def gemm_f16_nt_noalloc(a, b, c, stream=None):
     device before any stream capture.
     """
     m, n, k = _shape(a, b)
-    if tuple(c.shape) != (m, n) or not c.is_contiguous():
-        raise ValueError("c must be a contiguous float16 [M,N] tensor")
+    if c is None:
+        raise ValueError("c must be a contiguous float16 [M,N] CUDA tensor")
+    _check_matrix(c, m, n, "float16", "c")
     _check(lib().gemm_f16_nt_noalloc(m, n, k, _ptr(a), _ptr(b), _ptr(c), _stream(stream)), "gemm_f16_nt_noalloc")
     return c
 
@@ -290,6 +322,7 @@ def gemm_f16_nn_f32(a, b_kn, d=None, stream=None):
 
 def gemm_f16_nn_f32_ws(a, b_kn, d, workspace, stream=None):
     m, n, k = _shape_kn(a, b_kn)
+    _check_matrix(d, m, n, "float32", "d")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().gemm_f16_nn_f32_ws(m, n, k, _ptr(a), _ptr(b_kn), _ptr(d), _ptr(workspace), ws_bytes,
                                     _stream(stream)), "gemm_f16_nn_f32_ws")
@@ -304,9 +337,17 @@ def gemm_f16_nn_f32_plan_ex(m, n, k, variant=-1, raster_width=0, stream_k=-1):
 
 
 def gemm_f16_nt_host(a_host, b_host, c_host, a_dev, b_dev, c_dev, workspace=None, stream=None):
-    """End-to-end call on host tensors (pinned for asynchronous copies)."""
+    """End-to-end call on host tensors (pinned for asynchronous copies) and device buffers of the same
+    shapes; every host and device matrix is checked before the call."""
     m, k = a_host.shape
     n = b_host.shape[0]
+    for t, rows, cols, what in ((a_host, m, k, "a_host"), (b_host, n, k, "b_host"), (c_host, m, n, "c_host")):
+        if (tuple(t.shape) != (rows, cols) or str(t.dtype) != "torch.float16" or not t.is_contiguous()
+                or t.is_cuda):
+            raise ValueError("%s must be a contiguous float16 host tensor of shape [%d, %d]" % (what, rows, cols))
+    _check_matrix(a_dev, m, k, "float16", "a_dev")
+    _check_matrix(b_dev, n, k, "float16", "b_dev")
+    _check_matrix(c_dev, m, n, "float16", "c_dev")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().gemm_f16_nt_host(m, n, k, _ptr(a_host), _ptr(b_host), _ptr(c_host), _ptr(a_dev), _ptr(b_dev),
                                   _ptr(c_dev), _ptr(workspace), ws_bytes, _stream(stream)), "gemm_f16_nt_host")
@@ -321,6 +362,10 @@ def gemm_f16_take_device_error(stream=None):
 
 
 def gemm_f16_nt_run_stall_test(plan, a, b, c, skip_fill, wait_limit_cycles, stream=None):
+    m, n, k = int(plan.m), int(plan.n), int(plan.k)
+    _check_matrix(a, m, k, "float16", "a")
+    _check_matrix(b, n, k, "float16", "b")
+    _check_matrix(c, m, n, "float16", "c")
     return lib().gemm_f16_nt_run_stall_test(ctypes.byref(plan), _ptr(a), _ptr(b), _ptr(c), skip_fill,
                                             wait_limit_cycles, _stream(stream))
 
