@@ -236,9 +236,12 @@ bool rotate_pays(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks)
     return (tiles_m == 1 || tiles_n == 1) && k_blocks >= 8;
 }
 
+// Neither pays with fewer than 16 K blocks per tile: each cluster's K range is then a few blocks and
+// the partial fix-up costs more than the work it spreads (1024 x 1024 x 448, 7 K blocks: a tail over
+// 72 clusters took 9.05 us against 4.81 for the data-parallel 128 x 128 tiles).
 bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
 {
-    if (k_blocks < 4 || num_tiles * k_blocks < 2 * slots) return false;
+    if (k_blocks < 16 || num_tiles * k_blocks < 2 * slots) return false;
     return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
@@ -323,12 +326,19 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
         const int64_t s = slots_by_variant ? slots_by_variant[v] : num_sms / (kVariants[v].cg * kVariants[v].mc);
         return s < 1 ? 1 : s;
     };
-    if (m <= 128) return 2 * cdiv(n, 256) >= slots_of(13) ? 13 : 1;
-    // Small products whose 128 x 128 tiles fit one wave of single CTAs and whose K is too short to be
-    // split (fewer than 8 K blocks): the launch is latency-bound, and single CTAs halve each one's
-    // main loop and its share of C to store (256^3: 4.34 us per launch against 6.42 for the
-    // 256 x 256 pair tile, 5.00 for 128 x 256 and 5.80 for 256 x 128, back to back on GB300).
-    if (k_blocks < 8 && cdiv(m, 128) * cdiv(n, 128) <= int64_t(num_sms)) return 1;
+    // Small products with fewer than 8 K blocks whose single-CTA tiles fit one wave: the launch is
+    // latency-bound, and the smallest tile that still fits one wave shortens each CTA's main loop and
+    // its share of C to store.  Device time per launch on GB300 (CUDA graph, 128 x 64 / 128 x 128 /
+    // 256 x 256 pair): 256^3 3.66 / 3.89 / 5.74 us; 512 x 512 x 256 3.45 / 3.92; 256 x 1024 x 384
+    // 4.02 / 4.47; 128 x 2048 x 256 3.48 / 3.95; 1024 x 1024 x 448 4.62 / 4.81.  Once the 128 x 64
+    // tiles need a second wave they lose (2048 x 1024 x 256: 5.01 against 4.08).
+    const bool short_k = k_blocks < 8;
+    if (m <= 128) {
+        if (short_k && cdiv(n, 64) <= int64_t(num_sms)) return 18;
+        return 2 * cdiv(n, 256) >= slots_of(13) ? 13 : 1;
+    }
+    if (short_k && cdiv(m, 128) * cdiv(n, 64) <= int64_t(num_sms)) return 18;
+    if (short_k && cdiv(m, 128) * cdiv(n, 128) <= int64_t(num_sms)) return 1;
     if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
     const int64_t pair_tiles_m = cdiv(m, 256), tiles_n = cdiv(n, 256);
     int32_t alt = 2;

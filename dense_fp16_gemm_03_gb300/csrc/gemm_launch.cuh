@@ -119,6 +119,7 @@ const Variant kVariants[] = {
     GEMM_VARIANT_WIDE(4, 224),  // 16: 256 x 448 (fills the last wave where N / 512 would leave it idle)
     GEMM_VARIANT_WIDE(5, 160),  // 17: 256 x 320, five stages (4096^3: 208 tiles, 2.7 waves, where 512 columns
                                 //     make 128 tiles, 1.7 waves)
+    GEMM_VARIANT(1, 64, 8, 1),  // 18: 128 x 64 tile, one CTA (small, latency-bound products)
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 

@@ -142,7 +142,7 @@ typedef struct gemm_f16_plan {
  * 128 x block_n fp32.  Unlike the stream-K tail, no one cluster adds many
  * parts, so a tile's K can be spread over the whole GPU.  Variants with
  * fp16 C, B [N,K], tiles of whole 64-column chunks up to 256 columns and no
- * operand swap only (0-4, 11, 12).
+ * operand swap only (0-4, 11, 12, 18).
  */
 
 /* Human-readable name of a status code (static string, never NULL).  No

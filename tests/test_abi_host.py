@@ -166,7 +166,7 @@ def test_no_cuda_device_is_an_error_not_a_crash(L):
 
 @pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 4096), (128, 16384, 16384), (8192, 8192, 8192),
                                    (1000, 1000, 1000), (128, 256, 8192)])
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15, 16, 17])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 11, 12, 13, 14, 15, 16, 17, 18])
 def test_stream_k_plan_invariants(L, shape, variant):
     m, n, k = shape
     for sms in (148, 152):
@@ -230,7 +230,7 @@ def test_gb300_plans_of_the_configured_workloads(L):
     lines), and the committed DRAM-traffic captures were taken on exactly those plans."""
     import json
     expect = {
-        "square_256": (1, 0, 0, 0),
+        "square_256": (18, 0, 0, 0),
         "square_4096": (15, 0, 0, 0),
         "square_8192": (15, 0, 0, 0),
         "ragged_3000x5000x4096": (16, 0, 0, 0),
@@ -343,8 +343,11 @@ def test_k_rotation_rule(L):
     ((3000, 5000, 4096), 4, 1, False),     # with 38 clusters of four, multicast pairs and a stream-K tail
                                            # (3.3 waves) edge out 144 tiles of 256 x 448 (95% of 2 waves);
                                            # GB300 fits 36, and there the 256 x 448 tile wins
-    ((256, 256, 256), 1, 0, False),        # latency-bound: four single-CTA 128 x 128 tiles (4.34 us against 6.42
-                                           # for one 256 x 256 pair tile)
+    ((256, 256, 256), 18, 0, False),       # latency-bound: eight single-CTA 128 x 64 tiles (3.66 us against 3.89
+                                           # for 128 x 128 and 5.74 for one 256 x 256 pair tile)
+    ((2048, 1024, 256), 1, 0, False),      # 128 x 64 tiles would need a second wave: 128 x 128
+    ((1024, 1024, 448), 18, 0, False),     # 7 K blocks: no stream-K tail (it took 9.05 us against 4.6)
+    ((128, 2048, 256), 18, 0, False),      # a strip of rows with short K
     ((256, 256, 512), 2, 0, False),        # eight K blocks: the pair tile as before
     ((128, 16384, 16384), 13, 0, False),   # M <= 128, B rows for 64 of 76 pairs: swapped pair tiles, rotated
     ((100, 20000, 8192), 13, 1, False),    # 79 pair tiles for 76 pairs: a stream-K tail, not a second wave

@@ -17,7 +17,7 @@ from dense_fp16_gemm_03_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-SPLIT_VARIANTS = [0, 1, 2, 3, 4, 11, 12]   # fp16 C, B [N,K], whole 64-column chunks, no operand swap
+SPLIT_VARIANTS = [0, 1, 2, 3, 4, 11, 12, 18]   # fp16 C, B [N,K], whole 64-column chunks, no operand swap
 SHAPES = [(129, 264, 2048), (300, 520, 4096), (640, 1032, 520), (1000, 1000, 1000), (2304, 2304, 1024),
           (3000, 5000, 512), (8, 64, 8192)]
 
