@@ -236,12 +236,14 @@ bool rotate_pays(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks)
     return (tiles_m == 1 || tiles_n == 1) && k_blocks >= 8;
 }
 
-// Neither pays with fewer than 16 K blocks per tile: each cluster's K range is then a few blocks and
-// the partial fix-up costs more than the work it spreads (1024 x 1024 x 448, 7 K blocks: a tail over
-// 72 clusters took 9.05 us against 4.81 for the data-parallel 128 x 128 tiles).
+// Neither pays with 32 K blocks per tile or fewer: each cluster's K range is then short and the
+// partial fix-up (and, for split K, the reduction launch) costs more than the work it spreads.
+// Device time on GB300 against the best data-parallel plan: 1024 x 1024 x 448 (7 K blocks) 9.05
+// against 4.62 us; 1024^3 (16) 12.16 (tail) and 9.82 (split) against 6.89; 2048^3 (32) 22.19 and
+// 27.16 against 13.30.  Every tail and split measured to pay had 47 K blocks or more.
 bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
 {
-    if (k_blocks < 16 || num_tiles * k_blocks < 2 * slots) return false;
+    if (k_blocks <= 32 || num_tiles * k_blocks < 2 * slots) return false;
     return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
@@ -341,6 +343,15 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
     if (short_k && cdiv(m, 128) * cdiv(n, 128) <= int64_t(num_sms)) return 1;
     if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
     const int64_t pair_tiles_m = cdiv(m, 256), tiles_n = cdiv(n, 256);
+    // Mid-size products (up to 32 K blocks) whose 256 x 256 pair tiles would not fill one wave: the
+    // smallest single-CTA tile that still fits one wave, data-parallel.  Device time per launch on
+    // GB300 (CUDA graph; this choice / the best other plan / the pair or multicast tile with split K
+    // chosen before): 512^3 4.39 / 4.84 / 6.95 us, 1024^3 6.91 / 6.89 / 13.09, 1536^3 9.56 / 9.96 /
+    // 18.46, 2048^3 13.30 / 15.20 / 15.42, 1024 x 2048 x 512 5.25 / 5.74 / 7.02.
+    if (k_blocks <= 32 && pair_tiles_m * tiles_n < slots_of(2)) {
+        for (int32_t v : {18, 1, 0})
+            if (cdiv(m, 128) * cdiv(n, kVariants[v].bn) <= int64_t(num_sms)) return v;
+    }
     int32_t alt = 2;
     int64_t alt_tiles_m = pair_tiles_m;
     if (m > 256 && wave_efficiency(pair_tiles_m * tiles_n, slots_of(2)) < 0.95) {

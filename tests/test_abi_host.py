@@ -348,7 +348,10 @@ def test_k_rotation_rule(L):
     ((2048, 1024, 256), 1, 0, False),      # 128 x 64 tiles would need a second wave: 128 x 128
     ((1024, 1024, 448), 18, 0, False),     # 7 K blocks: no stream-K tail (it took 9.05 us against 4.6)
     ((128, 2048, 256), 18, 0, False),      # a strip of rows with short K
-    ((256, 256, 512), 2, 0, False),        # eight K blocks: the pair tile as before
+    ((256, 256, 512), 18, 0, False),       # mid-size, 8 K blocks: the smallest single-CTA tile in one wave
+    ((1024, 1024, 1024), 18, 0, False),    # (1024^3: 6.91 us against 13.09 for multicast pairs with split K)
+    ((1536, 1536, 1536), 1, 0, False),     # 128 x 64 tiles would need two waves: 128 x 128
+    ((2048, 2048, 2048), 0, 0, False),     # 128 x 256 (13.30 us against 15.42)
     ((128, 16384, 16384), 13, 0, False),   # M <= 128, B rows for 64 of 76 pairs: swapped pair tiles, rotated
     ((100, 20000, 8192), 13, 1, False),    # 79 pair tiles for 76 pairs: a stream-K tail, not a second wave
     ((128, 8192, 8192), 1, 0, True),       # 32 pair tiles would idle most pairs: 128 x 128 tiles, K split

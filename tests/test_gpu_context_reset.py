@@ -69,8 +69,8 @@ CHILD = textwrap.dedent(r'''
         if not np.array_equal(out, ref):
             raise SystemExit("%s differs from the oracle (%d elements)" % (fn_name, int((out != ref).sum())))
 
-    # 100 x 20000 x 2048 needs scratch (a stream-K tail): the allocation-free form uses the static array
-    A1, B1 = inputs.make_operands(100, 20000, 2048, "eighths", seed=3)
+    # 100 x 20000 x 4104 needs scratch (a stream-K tail): the allocation-free form uses the static array
+    A1, B1 = inputs.make_operands(100, 20000, 4104, "eighths", seed=3)
     A2, B2 = inputs.make_operands(300, 520, 264, "eighths", seed=4)
     for round_ in range(2):
         run("gemm_f16_nt_noalloc", A1, B1)

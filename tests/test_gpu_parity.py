@@ -109,10 +109,10 @@ def test_stream_k_exact(shape, variant):
 
 @pytest.mark.parametrize("variant", [1, 13])
 def test_stream_k_tail_past_one_wave_exact(variant):
-    """A few more tiles than clusters (one row of them, K in 17 blocks, the last ragged): the automatic
+    """A few more tiles than clusters (one row of them, K in 33 blocks, the last ragged): the automatic
     tail spreads every tile over all clusters, each taking a little over one tile, so nearly every
     tile is split in two and finished by the cluster that holds its first K block."""
-    M, N, K = 100, 128 * (num_sms() + 6), 1032
+    M, N, K = 100, 128 * (num_sms() + 6), 2056
     plan = G.gemm_f16_nt_plan_ex(M, N, K, variant, 0, -1)
     assert plan.stream_k == 1 and plan.dp_tiles == 0 and plan.num_tiles > plan.grid // plan.cluster
     A, B = inputs.make_operands(M, N, K, "eighths", seed=N + variant)
@@ -167,7 +167,7 @@ def test_stream_k_plan_shape():
 
 
 def test_workspace_entry_point_rejects_small_workspace():
-    M, N, K = 1000, 1000, 1000
+    M, N, K = 1000, 1000, 4096
     need = G.gemm_f16_nt_workspace_size(M, N, K)
     assert need > 0                               # the automatic plan splits K here (few tiles)
     a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
