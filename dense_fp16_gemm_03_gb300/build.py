@@ -26,22 +26,37 @@ FLAGS = [
 ]
 
 
-def _stale():
-    if not os.path.exists(LIB):
+def _stale_lib(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in DEPS)
+
+
+def _compile(lib, extra):
+    tmp = lib + ".tmp%d" % os.getpid()
+    subprocess.run([NVCC, *FLAGS, *extra, "-o", tmp, *SOURCES], check=True)
+    os.replace(tmp, lib)
+    return lib
 
 
 def build(force=False, verbose_ptxas=False):
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and not _stale():
+    if not force and not _stale_lib(LIB):
         return LIB
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [NVCC, *FLAGS, *(["-Xptxas", "-v"] if verbose_ptxas else []), "-o", tmp, *SOURCES]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    return _compile(LIB, ["-Xptxas", "-v"] if verbose_ptxas else [])
+
+
+# The measurement build with phase stamps in the single-CTA / CTA-pair kernel
+# (GEMM_F16_PHASE_TRACE; see gemm_f16_trace_set).  Never loaded by the product.
+TRACE_LIB = os.path.join(OUT_DIR, "libgemm_f16_trace.so")
+
+
+def build_trace(force=False):
+    os.makedirs(OUT_DIR, exist_ok=True)
+    if not force and not _stale_lib(TRACE_LIB):
+        return TRACE_LIB
+    return _compile(TRACE_LIB, ["-DGEMM_F16_PHASE_TRACE"])
 
 
 if __name__ == "__main__":

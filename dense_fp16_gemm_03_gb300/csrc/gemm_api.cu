@@ -29,6 +29,11 @@ using namespace gemm_f16;
 // read and cleared by gemm_f16_take_device_error.
 __device__ uint32_t g_gemm_f16_error_word = 0u;
 
+#ifdef GEMM_F16_PHASE_TRACE
+// Phase-trace buffer of the following launches (trace build only).
+static std::atomic<unsigned long long *> g_trace_buffer{nullptr};
+#endif
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -636,6 +641,9 @@ gemm_status_t launch_plan(const gemm_f16_plan_t &plan, const DeviceInfo *dev, co
     KernelParams params;
     memset(&params, 0, sizeof(params));
     st = encode_tensor_maps(var, plan, a, b, c, &params);
+#ifdef GEMM_F16_PHASE_TRACE
+    params.trace = g_trace_buffer.load();
+#endif
     if (st != GEMM_OK) return st;
     // kernel-side problem: the transposed one for a swapped variant
     const int64_t km = var.swap ? plan.n : plan.m;
@@ -705,6 +713,13 @@ const char *gemm_status_string(gemm_status_t s)
 {
     return gemm_f16_status_string(s);
 }
+
+#ifdef GEMM_F16_PHASE_TRACE
+void gemm_f16_trace_set(unsigned long long *buffer)
+{
+    g_trace_buffer.store(buffer);
+}
+#endif
 
 int32_t gemm_f16_variant_count(void)
 {

@@ -113,7 +113,40 @@ struct KernelParams {
                           // of CTA 0 leaves undone, to exercise the bounded waits; ~0u = none
     long long wait_limit; // cycles a single barrier wait may take before it gives up
     uint32_t *error_word;
+#ifdef GEMM_F16_PHASE_TRACE
+    unsigned long long *trace;  // null, or kTraceSlots global-timer stamps per CTA
+#endif
 };
+
+// Phase trace (a separate build with GEMM_F16_PHASE_TRACE defined; compiled out otherwise): one
+// thread per phase stores %globaltimer (ns) into its CTA's slot each time it passes the phase, so a
+// CTA that runs several segments keeps its last segment's stamps.  The store is not waited on;
+// reading the slot first would put a global-load round trip into the traced thread's path.
+enum TracePhase : int {
+    kTraceEntry = 0,       // thread 0 enters the kernel
+    kTraceSetUp = 1,       // barriers initialised, tensor memory allocated, CTA (cluster) synchronised
+    kTraceDepWait = 2,     // the previous launch in the stream has completed (griddepcontrol.wait)
+    kTraceFirstFull = 3,   // the MMA issuer sees a segment's first ring stage full
+    kTraceMmaDone = 4,     // a segment's last MMA is committed
+    kTraceAccReady = 5,    // the epilogue sees a segment's accumulator complete
+    kTraceStored = 6,      // a segment's stores (or published partial) are issued
+    kTraceStoresDone = 7,  // the epilogue's bulk stores have all completed
+    kTraceTeardown = 8,    // the teardown barrier is passed
+    kTraceExit = 9,        // tensor memory is freed; the CTA exits
+    kTraceSlots = 16,
+};
+#ifdef GEMM_F16_PHASE_TRACE
+__device__ __forceinline__ void trace_mark(const KernelParams &p, int phase)
+{
+    if (p.trace == nullptr) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[size_t(blockIdx.x) * kTraceSlots + phase] = t;
+}
+#define GEMM_TRACE(phase) trace_mark(p, phase)
+#else
+#define GEMM_TRACE(phase) ((void)0)
+#endif
 
 template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true, bool C_TRANS = false,
           int EPI = 2>
@@ -410,6 +443,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::kOffTmemSlot);
     volatile uint32_t *fills_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffFills);
+    if (threadIdx.x == 0) GEMM_TRACE(kTraceEntry);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -438,6 +472,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) GEMM_TRACE(kTraceSetUp);
 
     // Where this CTA's boxes of a segment start: the A rows m0, the B rows (or, B stored [K, N], the
     // columns) n0, and the K-walk rotation.  With k_rotate, a whole tile walks its K blocks from a
@@ -461,8 +496,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     // L2 to prefetch the boxes of its first ring fills: a prefetch is a hint with no effect on
     // results (L2 is where every write lands, so a line the previous kernel writes afterwards is
     // still read as written), and it lets this launch's first reads from DRAM overlap the previous
-    // launch's last tiles.
-    ptx::griddep_launch_dependents();
+    // launch's last tiles.  The next launch in the stream is let in once this CTA's first
+    // accumulator is complete (the epilogue below), not here: triggered at entry, every launch of a
+    // long run of small products becomes resident at once, each waiting on its predecessor, and
+    // the hand-over from one to the next slows down (one-tile launches replayed from a CUDA graph:
+    // 2.51 against 2.32 us at 64^3, 3.71 against 3.43 us at 256^3; level from 512^3 up).
     if (warp == 0 && lane == 0) {
         for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
             int32_t m0, n0;
@@ -484,6 +522,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         });
     }
     ptx::griddep_wait();
+    if (threadIdx.x == 0) GEMM_TRACE(kTraceDepWait);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -564,6 +603,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 for (uint32_t kb = k_lo; kb < k_hi; ++kb) {
                     if (!wait_bounded<CS>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
                     ptx::tc_fence_after_sync();
+                    if (kb == k_lo) GEMM_TRACE(kTraceFirstFull);
                     const uint64_t a_desc = smem_desc_sw128(base + Cfg::kOffA + stage * Cfg::kABytes);
                     const uint32_t b_addr = base + Cfg::kOffB + stage * Cfg::kBBytes;
                     const uint64_t b_desc = B_KMAJOR ? smem_desc_sw128(b_addr) : smem_desc_sw128_mn(b_addr);
@@ -586,6 +626,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 }
                 if constexpr (CG == 1) ptx::mma_commit(bar_acc_full(acc));
                 else ptx::mma_commit_pair(bar_acc_full(acc), uint16_t(0x3u << pair_leader));
+                GEMM_TRACE(kTraceMmaDone);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -612,6 +653,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         constexpr uint32_t kChunkFloats = 32u * kStoreCols;  // one warp's 32 x 64 piece
         const bool first_epi_thread = (threadIdx.x == 64u);
         uint32_t acc = 0, acc_phase = 0, stores = 0;
+        bool released = false;
         for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
@@ -625,6 +667,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             const bool all_ok = split ? ptx::named_barrier_and(1, 32 * kEpiWarps, ok) : __all_sync(0xffffffffu, ok);
             if (!all_ok) return false;
             ptx::tc_fence_after_sync();
+            if (!released) {
+                ptx::griddep_launch_dependents();  // the first accumulator is ready
+                released = true;
+            }
+            if (first_epi_thread) GEMM_TRACE(kTraceAccReady);
             const uint32_t acc_col = tmem_base + acc * Cfg::kAccCols + lane_sel;
             // Partial-tile layout in the workspace: per warp quarter and 64-column chunk, 16 float4
             // slots x 32 lanes, so every warp-wide 16-byte access is one contiguous 512-byte run.
@@ -793,6 +840,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     if constexpr (Cfg::kTail) store(std::integral_constant<int, 32>{}, Cfg::kFullChunks);
                 }
             }
+            if (first_epi_thread) GEMM_TRACE(kTraceStored);
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -806,14 +854,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             return true;
         });
         if (lane == 0) ptx::bulk_wait_group<0>();
+        if (threadIdx.x == 64u) GEMM_TRACE(kTraceStoresDone);
     }
 
     // ---------------------------------------------------- teardown
+    ptx::griddep_launch_dependents();  // a CTA whose epilogue stored nothing still lets the next launch in
     __syncwarp();
     ptx::tc_fence_before_sync();
     if constexpr (CS > 1) ptx::cluster_sync();
     else __syncthreads();
     ptx::tc_fence_after_sync();
+    if (threadIdx.x == 0) GEMM_TRACE(kTraceTeardown);
     // Between two cluster barriers every CTA of the cluster is still running, so the owners of full
     // barriers may read the other CTAs' flags: after an abort anywhere in the cluster they wait for
     // the ring loads still in flight before any CTA exits.
@@ -821,6 +872,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         nt_abort_drain<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>(p);
     if constexpr (CS > 1) ptx::cluster_sync();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
+    if (threadIdx.x == 32u) GEMM_TRACE(kTraceExit);
 }
 
 // Split-K reduction: for every tile, adds its split_k fp32 parts in part

@@ -354,6 +354,28 @@ gemm_status_t gemm_f16_nt_run_stall_test(const gemm_f16_plan_t *plan, const void
                                          void *c, uint32_t skip_fill, long long wait_limit_cycles,
                                          gemm_stream_t stream);
 
+#ifdef GEMM_F16_PHASE_TRACE
+/*
+ * Phase trace (only in the library built with GEMM_F16_PHASE_TRACE defined,
+ * a measurement build; the product build has neither this function nor the
+ * stamps).  Sets the device buffer that the single-CTA / CTA-pair kernel
+ * launched by the following calls in this process writes its
+ * phase stamps into, or NULL to stop.  Layout: 16 unsigned 64-bit slots per
+ * CTA of the launch (slot = CTA index * 16 + phase), each overwritten with
+ * %globaltimer (ns) every time its phase is passed, so a CTA that runs
+ * several tiles keeps its last tile's stamps and a slot still 0 (the caller
+ * zeroes the buffer) was not reached; give one buffer per traced launch.
+ * Phases 0..9: kernel entry; set-up done; previous launch complete; a tile's
+ * first ring stage full; its MMAs committed; its accumulator ready; its
+ * stores issued; all bulk stores complete; teardown barrier; exit.  The
+ * buffer is owned by the caller and
+ * must hold grid * 16 slots and stay allocated until the traced launches
+ * have completed.  The wide-tile kernel is not traced.  The pointer is
+ * captured at launch time (a CUDA graph keeps the value of its capture).
+ */
+void gemm_f16_trace_set(unsigned long long *buffer);
+#endif
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,9 +24,15 @@ def L():
     return G.lib()
 
 
-def _declared_functions():
+TRACE_BLOCK = re.compile(r"#ifdef GEMM_F16_PHASE_TRACE\n(.*?)#endif", re.S)
+
+
+def _declared_functions(trace_build=False):
+    """Functions the header declares for the product build (or, trace_build, only those of the trace build)."""
     text = open(os.path.join(ROOT, "include", "gemm_f16.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    blocks = TRACE_BLOCK.findall(text)
+    text = " ".join(blocks) if trace_build else TRACE_BLOCK.sub("", text)
     return sorted(set(re.findall(r"\b(gemm_\w+)\s*\(", text)))
 
 
@@ -36,6 +42,13 @@ def test_every_declared_symbol_is_exported(L):
     for name in names:
         assert hasattr(L, name), name
     assert set(names) == set(G.EXPORTED)
+
+
+def test_trace_entry_only_in_trace_build(L):
+    # the phase-trace setter is declared for the GEMM_F16_PHASE_TRACE build alone; the product
+    # library neither exports it nor carries the stamps
+    assert _declared_functions(trace_build=True) == ["gemm_f16_trace_set"]
+    assert not hasattr(L, "gemm_f16_trace_set")
 
 
 def test_static_scratch_size_matches_header(L):
