@@ -124,7 +124,7 @@ gemm_status_t device_info(DeviceInfo **out)
                     cudaGetLastError();
                     return GEMM_ERR_CUDA;
                 }
-                const int cs = var.cg * var.mc;
+                const int cs = cluster_of(var);
                 made.max_clusters[v] = sms / cs;
                 if (cs > 1) {
                     cudaLaunchConfig_t cfg;
@@ -245,10 +245,12 @@ bool rotate_pays(int64_t tiles_m, int64_t tiles_n, int64_t k_blocks)
 // partial fix-up (and, for split K, the reduction launch) costs more than the work it spreads.
 // Device time on GB300 against the best data-parallel plan: 1024 x 1024 x 448 (7 K blocks) 9.05
 // against 4.62 us; 1024^3 (16) 12.16 (tail) and 9.82 (split) against 6.89; 2048^3 (32) 22.19 and
-// 27.16 against 13.30.  Every tail and split measured to pay had 47 K blocks or more.
+// 27.16 against 13.30.  Every tail and split measured to pay had 47 K blocks or more.  With more,
+// even very few tiles are split (the parts keep at least 4 K blocks each): two 128 x 128 tiles with
+// K = 8192 would otherwise run on two SMs.
 bool streamk_pays(int64_t num_tiles, int64_t k_blocks, int64_t slots)
 {
-    if (k_blocks <= 32 || num_tiles * k_blocks < 2 * slots) return false;
+    if (k_blocks <= 32) return false;
     return wave_efficiency(num_tiles, slots) < 0.86;
 }
 
@@ -330,7 +332,7 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
 {
     if (layout == 1) return m <= 128 ? 6 : 7;  // B stored [K, N], fp32 result
     auto slots_of = [&](int v) -> int64_t {
-        const int64_t s = slots_by_variant ? slots_by_variant[v] : num_sms / (kVariants[v].cg * kVariants[v].mc);
+        const int64_t s = slots_by_variant ? slots_by_variant[v] : num_sms / cluster_of(kVariants[v]);
         return s < 1 ? 1 : s;
     };
     // Small products with fewer than 8 K blocks whose single-CTA tiles fit one wave: the launch is
@@ -340,6 +342,23 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
     // 4.02 / 4.47; 128 x 2048 x 256 3.48 / 3.95; 1024 x 1024 x 448 4.62 / 4.81.  Once the 128 x 64
     // tiles need a second wave they lose (2048 x 1024 x 256: 5.01 against 4.08).
     const bool short_k = k_blocks < 8;
+    // Few tiles and 16 to 64 K blocks: each SM brings in its operand boxes at a fixed rate (~90
+    // GB/s), so a launch whose tiles fit one wave is as long as one tile's K loop.  Sharing each
+    // tile's K blocks across a cluster (K split: 4 CTAs of 128 x 64, 2 of 128 x 64 or 2 of 128 x 128)
+    // shortens it, at ~2 us for the exchange of partials.  Device time per launch on GB300 (CUDA
+    // graph; this choice / the plan chosen before): 256 x 256 x 2048 6.08 / 10.16 us,
+    // 128 x 1024 x 2048 6.27 / 10.65, 512 x 512 x 1024 5.54 / 6.30, 512 x 512 x 2048 7.02 / 10.35,
+    // 512 x 1024 x 2048 8.32 / 10.45, 768 x 768 x 2048 8.61 / 10.46, 1024 x 1024 x 2048 9.45 / 10.91,
+    // 1024 x 1024 x 4096 13.45 / 16.59.  It lost with fewer K blocks (512^3 4.63 / 4.31; 1024^3 on
+    // 128 x 128 pairs 8.57 / 6.89) and, with more than 64, to a split K over all the SMs
+    // (256 x 256 x 8192 11.98 against 8.29 us).
+    if (k_blocks >= 16 && k_blocks <= 64) {
+        const int64_t tiles64 = cdiv(m, 128) * cdiv(n, 64), tiles128 = cdiv(m, 128) * cdiv(n, 128);
+        if (k_blocks >= 24 && tiles64 <= slots_of(19)) return 19;
+        if ((k_blocks >= 24 || 2 * tiles64 <= slots_of(20)) && tiles64 <= slots_of(20)) return 20;
+        // (one strip of A rows keeps its split K over more SMs: 100 x 5000 x 3000 12.86 against 13.65 us)
+        if (k_blocks >= 32 && m > 128 && tiles128 <= slots_of(21)) return 21;
+    }
     if (m <= 128) {
         if (short_k && cdiv(n, 64) <= int64_t(num_sms)) return 18;
         return 2 * cdiv(n, 256) >= slots_of(13) ? 13 : 1;
@@ -406,7 +425,7 @@ int64_t splitk_workspace_bytes(int64_t tiles, int64_t parts, int32_t cluster, in
 // 256 columns (not the wide tiles).
 bool split_capable(const Variant &var)
 {
-    return var.layout == 0 && !var.swap && var.bn % 64 == 0 && var.bn <= 256;
+    return var.layout == 0 && !var.swap && var.bn % 64 == 0 && var.bn <= 256 && var.ks == 1;
 }
 
 // Parts per tile: about one (tile, part) per resident cluster, each part at least 4 K blocks; a
@@ -450,7 +469,7 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     if (variant < 0) variant = auto_variant(m, n, cdiv(k, kBlockK), num_sms, slots_by_variant, layout < 0 ? 0 : layout);
     const Variant &var = kVariants[variant];
     if (layout >= 0 && var.layout != layout) return GEMM_ERR_INVALID_ARG;
-    const int32_t cs = var.cg * var.mc;  // CTAs per cluster
+    const int32_t cs = cluster_of(var);  // CTAs per cluster
     int32_t max_clusters = max_clusters_in > 0 ? max_clusters_in : num_sms / cs;
     if (slots_by_variant) max_clusters = slots_by_variant[variant];
     gemm_f16_plan_t p;
@@ -493,6 +512,11 @@ gemm_status_t make_plan(int64_t m, int64_t n, int64_t k, int32_t num_sms, int32_
     if (wide) {
         tail = wide_tail_pays(p.num_tiles, p.k_blocks, slots);
         rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks) && !tail;
+    }
+    if (var.ks > 1) {
+        // K split: whole tiles only, data-parallel (the cluster already shares each tile's K blocks)
+        if (stream_k == 1 || stream_k == 2) return GEMM_ERR_INVALID_ARG;
+        tail = false;
     }
     if (stream_k == 0) rotate = rotate_pays(p.tiles_m, p.tiles_n, p.k_blocks);
     if (stream_k == 1) rotate = false;
@@ -578,6 +602,7 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
         return GEMM_ERR_INVALID_ARG;
     const int64_t workers = plan.grid / plan.cluster;
     if (plan.k_rotate != 0 && plan.k_rotate != 1) return GEMM_ERR_INVALID_ARG;
+    if (kVariants[plan.variant].ks > 1 && (plan.stream_k != 0 || plan.split_k > 1)) return GEMM_ERR_INVALID_ARG;
     if (plan.split_k > 1) {
         // clusters walk the (tile, part) units persistently and wait for nobody: any grid works
         if (plan.stream_k != 0 || !split_capable(kVariants[plan.variant]) || plan.dp_tiles != plan.num_tiles ||
@@ -727,11 +752,13 @@ int32_t gemm_f16_variant_count(void)
 }
 
 gemm_status_t gemm_f16_variant_info(int32_t v, int32_t *cta_group, int32_t *block_n, int32_t *stages,
-                                    int32_t *smem_bytes, int32_t *cluster, int32_t *layout, int32_t *swapped)
+                                    int32_t *smem_bytes, int32_t *cluster, int32_t *layout, int32_t *swapped,
+                                    int32_t *k_split)
 {
     if (v < 0 || v >= kNumVariants) return GEMM_ERR_INVALID_ARG;
+    if (k_split) *k_split = kVariants[v].ks;
     if (swapped) *swapped = kVariants[v].swap;
-    if (cluster) *cluster = kVariants[v].cg * kVariants[v].mc;
+    if (cluster) *cluster = cluster_of(kVariants[v]);
     if (layout) *layout = kVariants[v].layout;
     if (cta_group) *cta_group = kVariants[v].cg;
     if (block_n) *block_n = kVariants[v].bn;

@@ -91,6 +91,8 @@ enum : uint32_t {
     kErrWaitDrain = 5,
     kErrWaitPartial = 6,
     kErrWaitRingDrain = 7,   // after an abort, a ring stage's loads did not all land in time
+    kErrWaitRecv = 8,        // K split: the partners' partial slices of a tile did not arrive in time
+    kErrWaitPeerFree = 9,    // K split: the partners did not free their receive slots in time
 };
 
 struct KernelParams {
@@ -113,6 +115,7 @@ struct KernelParams {
                           // of CTA 0 leaves undone, to exercise the bounded waits; ~0u = none
     long long wait_limit; // cycles a single barrier wait may take before it gives up
     uint32_t *error_word;
+    void *c_out;          // C [M, N] fp16, row-major (the K-split epilogue stores it directly)
 #ifdef GEMM_F16_PHASE_TRACE
     unsigned long long *trace;  // null, or kTraceSlots global-timer stamps per CTA
 #endif
@@ -133,6 +136,8 @@ enum TracePhase : int {
     kTraceStoresDone = 7,  // the epilogue's bulk stores have all completed
     kTraceTeardown = 8,    // the teardown barrier is passed
     kTraceExit = 9,        // tensor memory is freed; the CTA exits
+    kTraceKsSent = 10,     // K split: a tile's partner slices are sent
+    kTraceKsReceived = 11, // K split: the partners' slices of a tile have arrived
     kTraceSlots = 16,
 };
 #ifdef GEMM_F16_PHASE_TRACE
@@ -148,16 +153,26 @@ __device__ __forceinline__ void trace_mark(const KernelParams &p, int phase)
 #define GEMM_TRACE(phase) ((void)0)
 #endif
 
+// KS > 1 (K split): a cluster of KS single CTAs computes one 128 x BN tile, CTA r accumulating the
+// r-th of KS runs of the tile's K blocks; the CTAs then trade fp32 partials through distributed
+// shared memory so that CTA r adds all KS partials of columns [r BN / KS, (r + 1) BN / KS) and
+// stores them.  It lets the K blocks of few tiles be loaded by more SMs at once: each SM brings in
+// its operand boxes at a fixed rate, which bounds a launch with fewer tiles than SMs.
 template <int CG, int BN, int STAGES, int MC = 1, bool B_KMAJOR = true, bool C_F16 = true, bool C_TRANS = false,
-          int EPI = 2>
+          int EPI = 2, int KS = 1>
 struct KernelCfg {
     static_assert(CG == 1 || CG == 2, "cta group");
     static_assert(MC == 1 || MC == 2 || MC == 4, "cluster multicast width");
+    static_assert(KS == 1 || KS == 2 || KS == 4, "K split across the cluster");
+    static_assert(KS == 1 || (CG == 1 && MC == 1 && B_KMAJOR && C_F16 && !C_TRANS), "K split: single-CTA fp16 tiles");
     static constexpr bool kAMC = (CG == 1 && MC > 1);  // single CTAs along N share A by multicast
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile N");
     static constexpr int kFullChunks = BN / 64;      // 64-column epilogue chunks
     static constexpr bool kTail = (BN % 64) != 0;   // plus one 32-column chunk
-    static constexpr int kCS = CG * MC;             // CTAs per cluster
+    static constexpr int kCS = CG * MC * KS;        // CTAs per cluster
+    static constexpr int kKsCols = BN / KS;         // K split: columns of a tile one CTA adds up and stores
+    static_assert(KS == 1 || (BN % 64 == 0 && kKsCols % 16 == 0), "K split slices");
+    static constexpr int kRecvSlotBytes = 128 * kKsCols * 4;  // K split: one partner's fp32 slice of 128 rows
     static constexpr int kBM = 128 * CG;            // MMA M (one pair)
     static constexpr int kBMCluster = kAMC ? kBM : kBM * MC;  // output rows per scheduling unit
     static constexpr int kBNCluster = kAMC ? BN * MC : BN;    // output columns per scheduling unit
@@ -170,15 +185,24 @@ struct KernelCfg {
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + STAGES * kABytes;
     static constexpr int kOffStore = kOffB + STAGES * kBBytes;
-    static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, drain
+    // full, empty, acc_full x2, acc_empty x2, drain; K split: recv_full, peer_free
+    static constexpr int kNumBars = 2 * STAGES + 5 + (KS > 1 ? 2 : 0);
     // EPI staging buffers per epilogue warp: 2 lets a warp fill one while the other is being stored;
     // 1 frees 16 KB for one more ring stage
     static_assert(EPI == 1 || EPI == 2, "epilogue staging buffers");
-    static constexpr int kOffBar = kOffStore + kEpiWarps * EPI * kStoreBufBytes;
+    // K split: where the other variants stage their stores, one receive slot per partner (its slice
+    // of this CTA's columns) and one send slot per partner (this CTA's slice of the partner's
+    // columns, moved by bulk copies); C is stored from registers
+    static constexpr int kEpiBytes = KS > 1 ? 2 * (KS - 1) * kRecvSlotBytes : kEpiWarps * EPI * kStoreBufBytes;
+    static constexpr int kOffSend = kOffStore + (KS - 1) * kRecvSlotBytes;
+    static constexpr int kOffBar = kOffStore + kEpiBytes;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffFills = kOffAbort + 4;  // ring fills the producer walked (read by the abort drain)
-    static constexpr int kSmemUsed = kOffFills + 4;
+    // K split: tiles whose partner slices the epilogue armed / received (read by the abort drain)
+    static constexpr int kOffRecvArmed = kOffFills + 4;
+    static constexpr int kOffRecvDone = kOffRecvArmed + 4;
+    static constexpr int kSmemUsed = kOffFills + 4 + (KS > 1 ? 8 : 0);
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
     static constexpr int kAccCols = (BN + 63) / 64 * 64;  // accumulator buffer stride (64-column aligned)
     static constexpr int kTmemCols = (2 * kAccCols <= 128) ? 128 : (2 * kAccCols <= 256 ? 256 : 512);
@@ -378,19 +402,28 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
 // the cluster gave up a wait, wait for the ring loads still in flight.  Kept
 // out of line, and recomputing its addresses, so that it costs the main
 // loops no registers.
-template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI>
+template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI, int KS>
 __device__ __noinline__ void nt_abort_drain(const KernelParams &p)
 {
-    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>;
+    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI, KS>;
     constexpr int CS = Cfg::kCS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t cta_rank = (CS > 1) ? ptx::cluster_ctarank() : 0u;
-    const uint32_t pair = cta_rank / CG;
+    const uint32_t pair = (KS > 1) ? 0u : cta_rank / CG;
     uint32_t fills[CS];
     bool aborted = false;
-    if constexpr (CS > 1) {
+    if constexpr (KS > 1) {
+        // K split: no CTA loads into another's ring, and a CTA that did not give up received every
+        // partner slice sent to it, so this CTA's own state decides
+        aborted = *reinterpret_cast<volatile uint32_t *>(smem_raw + (base - raw) + Cfg::kOffAbort) != 0u;
+#pragma unroll
+        for (int x = 0; x < CS; ++x)
+            fills[x] = uint32_t(x) == cta_rank
+                           ? *reinterpret_cast<volatile uint32_t *>(smem_raw + (base - raw) + Cfg::kOffFills)
+                           : 0u;
+    } else if constexpr (CS > 1) {
 #pragma unroll
         for (int x = 0; x < CS; ++x) {
             aborted |= ptx::ld_shared_cluster_u32(ptx::map_to_rank(base + Cfg::kOffAbort, uint32_t(x))) != 0u;
@@ -403,18 +436,37 @@ __device__ __noinline__ void nt_abort_drain(const KernelParams &p)
     if (!aborted) return;
     // bytes one fill of cluster CTA x lands on this CTA's full barriers (see the producer)
     auto share = [&](uint32_t x) -> uint32_t {
-        if constexpr (Cfg::kAMC) return uint32_t(Cfg::kASlice * 128) + (x == cta_rank ? uint32_t(Cfg::kBBytes) : 0u);
+        if constexpr (KS > 1) return x == cta_rank ? uint32_t(Cfg::kABytes + Cfg::kBBytes) : 0u;  // own loads only
+        else if constexpr (Cfg::kAMC) return uint32_t(Cfg::kASlice * 128) + (x == cta_rank ? uint32_t(Cfg::kBBytes) : 0u);
         else if constexpr (MC == 1) return uint32_t(Cfg::kABytes + Cfg::kBBytes);
         else return ((x / CG) == pair ? uint32_t(Cfg::kABytes) : 0u) + uint32_t(Cfg::kBSlice * 128);
     };
     drain_ring<STAGES, CS>(base + Cfg::kOffBar, fills, cta_rank, blockIdx.x - cta_rank, uint32_t(Cfg::kStageTx),
                            share, p);
+    if constexpr (KS > 1) {
+        // Partners may have sent their slices of a tile whose arrival this CTA never waited for (the
+        // one after the last it received; they send the next only once it has summed the one before).
+        // Arm that phase if the epilogue did not and wait for it, bounded: it completes once every
+        // partner's bytes have landed, or the wait gives up.
+        const uint8_t *smem = smem_raw + (base - raw);
+        const uint32_t done = *reinterpret_cast<const volatile uint32_t *>(smem + Cfg::kOffRecvDone);
+        const uint32_t armed = *reinterpret_cast<const volatile uint32_t *>(smem + Cfg::kOffRecvArmed);
+        const uint32_t bar = base + Cfg::kOffBar + 8u * (2 * STAGES + 5);
+        if (armed == done) ptx::mbar_arrive_expect_tx(bar, uint32_t(KS - 1) * uint32_t(Cfg::kRecvSlotBytes));
+        const long long t0 = clock64();
+        while (!ptx::mbar_try_wait_cluster(bar, done & 1u)) {
+            if (clock64() - t0 > p.wait_limit) {
+                atomicCAS(p.error_word, 0u, kErrWaitRecv | (blockIdx.x << 8));
+                break;
+            }
+        }
+    }
 }
 
-template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI>
+template <int CG, int BN, int STAGES, int MC, bool B_KMAJOR, bool C_F16, bool C_TRANS, int EPI, int KS>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>;
+    using Cfg = KernelCfg<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI, KS>;
     constexpr int CS = Cfg::kCS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -424,8 +476,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t cta_rank = (CS > 1) ? ptx::cluster_ctarank() : 0u;  // rank in the cluster
-    const uint32_t pair_rank = (CG == 2) ? (cta_rank & 1u) : 0u;        // rank in the CTA pair
-    const uint32_t pair = cta_rank / CG;                                  // pair index in the cluster
+    const uint32_t ks_rank = (KS > 1) ? cta_rank : 0u;                  // K split: this CTA's run of K blocks
+    const uint32_t mc_rank = (KS > 1) ? 0u : cta_rank;                  // rank among CTAs sharing by multicast
+    const uint32_t pair_rank = (CG == 2) ? (mc_rank & 1u) : 0u;         // rank in the CTA pair
+    const uint32_t pair = mc_rank / CG;                                   // pair index in the cluster
     const uint32_t pair_leader = cta_rank - pair_rank;                    // cluster rank of the pair's first CTA
     const bool leader = (pair_rank == 0);
     const uint32_t cluster_id = blockIdx.x / CS;
@@ -456,6 +510,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             ptx::mbar_init(bar_acc_empty(b), kEpiWarps * CG);
         }
         ptx::mbar_init(bar_drain, 1);
+        if constexpr (KS > 1) {
+            ptx::mbar_init(base + Cfg::kOffBar + 8u * (2 * STAGES + 5), 1);  // recv_full: armed by the epilogue
+            // peer_free: one arrival per epilogue warp of every partner
+            ptx::mbar_init(base + Cfg::kOffBar + 8u * (2 * STAGES + 6), uint32_t(KS - 1) * kEpiWarps);
+            *reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffRecvArmed) = 0u;
+            *reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffRecvDone) = 0u;
+        }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&p.tmap_a);
@@ -489,6 +550,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         const bool whole = (k_lo == 0u) && (k_hi == p.k_blocks);
         rot = (p.k_rotate && whole) ? uint32_t((uint64_t(tile) * kRotateStride) % p.k_blocks) : 0u;
     };
+    // The K blocks [lo, hi) of a segment that this CTA loads and accumulates: all of them, or with a
+    // K split the ks_rank-th of KS contiguous runs of the walk (empty when the segment is shorter)
+    auto k_share = [&](uint32_t k_lo, uint32_t k_hi, uint32_t &lo, uint32_t &hi) {
+        if constexpr (KS > 1) {
+            const uint32_t len = k_hi - k_lo;
+            lo = k_lo + len * ks_rank / uint32_t(KS);
+            hi = k_lo + len * (ks_rank + 1u) / uint32_t(KS);
+        } else {
+            lo = k_lo;
+            hi = k_hi;
+        }
+    };
 
     // Launched as a programmatic dependent: the set-up above overlaps the tail of the previous
     // kernel in the stream, and nothing is read or written through the generic or the TMA load path
@@ -506,7 +579,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             int32_t m0, n0;
             uint32_t rot;
             segment_origin(tile, k_lo, k_hi, m0, n0, rot);
-            for (uint32_t kb = k_lo; kb < k_hi && kb < k_lo + uint32_t(STAGES); ++kb) {
+            uint32_t lo, hi;
+            k_share(k_lo, k_hi, lo, hi);
+            for (uint32_t kb = lo; kb < hi && kb < lo + uint32_t(STAGES); ++kb) {
                 uint32_t kr = kb + rot;
                 if (kr >= p.k_blocks) kr -= p.k_blocks;
                 const int32_t k0 = int32_t(kr * kBlockK);
@@ -533,7 +608,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 int32_t m0, n0;
                 uint32_t rot;
                 segment_origin(tile, k_lo, k_hi, m0, n0, rot);
-                for (uint32_t kb = k_lo; kb < k_hi; ++kb, ++fills) {
+                uint32_t lo, hi;
+                k_share(k_lo, k_hi, lo, hi);
+                for (uint32_t kb = lo; kb < hi; ++kb, ++fills) {
                     if (!wait_bounded<CS>(bar_empty(stage), phase ^ 1u, p, abort_flag, kErrWaitEmpty)) {
                         ok = false;
                         return false;
@@ -600,10 +677,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                     return false;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * Cfg::kAccCols;
-                for (uint32_t kb = k_lo; kb < k_hi; ++kb) {
+                uint32_t lo, hi;
+                k_share(k_lo, k_hi, lo, hi);
+                for (uint32_t kb = lo; kb < hi; ++kb) {
                     if (!wait_bounded<CS>(bar_full(stage), phase, p, abort_flag, kErrWaitFull)) return false;
                     ptx::tc_fence_after_sync();
-                    if (kb == k_lo) GEMM_TRACE(kTraceFirstFull);
+                    if (kb == lo) GEMM_TRACE(kTraceFirstFull);
                     const uint64_t a_desc = smem_desc_sw128(base + Cfg::kOffA + stage * Cfg::kABytes);
                     const uint32_t b_addr = base + Cfg::kOffB + stage * Cfg::kBBytes;
                     const uint64_t b_desc = B_KMAJOR ? smem_desc_sw128(b_addr) : smem_desc_sw128_mn(b_addr);
@@ -613,7 +692,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         ptx::mma_f16<CG>(d_tmem, a_desc + uint64_t(2 * kk), b_desc + kBStep * uint64_t(kk), idesc,
-                                         (kb != k_lo || kk != 0) ? 1u : 0u);
+                                         (kb != lo || kk != 0) ? 1u : 0u);
                     }
                     // the stage is free in every CTA whose producer writes into this pair's stage
                     if constexpr (Cfg::kAMC) ptx::mma_commit_mc(bar_empty(stage), uint16_t((1u << CS) - 1u));
@@ -654,6 +733,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
         const bool first_epi_thread = (threadIdx.x == 64u);
         uint32_t acc = 0, acc_phase = 0, stores = 0;
         bool released = false;
+        // K split: the partners' slots in this CTA, the barrier their bytes complete (armed once per
+        // tile) and the one on which the partners report that this CTA's slots in them are free again
+        const uint32_t recv_base = base + Cfg::kOffStore;
+        const uint32_t bar_recv_full = base + Cfg::kOffBar + 8u * (2 * STAGES + 5);
+        const uint32_t bar_peer_free = base + Cfg::kOffBar + 8u * (2 * STAGES + 6);
+        uint32_t recv_phase = 0, peer_phase = 0, ks_tiles = 0;
         for_each_segment(p, cluster_id, num_clusters, [&](uint32_t tile, uint32_t k_lo, uint32_t k_hi) {
             uint32_t mb, nb;
             raster_coord(p.raster, tile, mb, nb);
@@ -673,6 +758,136 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             }
             if (first_epi_thread) GEMM_TRACE(kTraceAccReady);
             const uint32_t acc_col = tmem_base + acc * Cfg::kAccCols + lane_sel;
+            if constexpr (KS > 1) {
+                // ---- K split: every CTA of the cluster holds a partial of the whole tile.  Send the
+                // partners their columns, keep this CTA's, add the KS partials of those in rank order
+                // (so the sum does not depend on which CTA finishes first) and store them.
+                constexpr int W = Cfg::kKsCols;
+                constexpr uint32_t kChunks = uint32_t(W) / 4u;  // 16-byte chunks of one row of a slice
+                const uint32_t row_local = quarter * 32u + lane;
+                const uint32_t len = k_hi - k_lo;
+                const bool have = len * (ks_rank + 1u) / uint32_t(KS) > len * ks_rank / uint32_t(KS);
+                // this thread's row, columns [j W, j W + W) of the partial (zero: no K block here)
+                auto slice = [&](uint32_t j, uint32_t (&v)[W]) {
+                    if (have) {
+                        if constexpr (W == 16) ptx::tmem_ld_32x32b_x16_wait(acc_col + j * uint32_t(W), v);
+                        else if constexpr (W == 32) ptx::tmem_ld_32x32b_x32_wait(acc_col + j * uint32_t(W), v);
+                        else ptx::tmem_ld_32x32b_x64_wait(acc_col + j * uint32_t(W), v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[i] = 0u;
+                    }
+                };
+                // a slot row holds the 16-byte chunks rotated by the row, so that a warp's accesses to
+                // one chunk of 32 consecutive rows spread over the banks
+                auto chunk_at = [&](uint32_t c) { return ((c ^ (row_local & (kChunks - 1u))) * 16u); };
+                // (each wait's outcome is made warp-uniform: the tensor-memory loads and __syncwarp
+                // below need the whole warp)
+                if (ks_tiles > 0u) {  // the partners have added up this CTA's previous slices
+                    const bool free_ok = wait_bounded<CS>(bar_peer_free, peer_phase, p, abort_flag, kErrWaitPeerFree);
+                    if (!__all_sync(0xffffffffu, free_ok)) return false;
+                    peer_phase ^= 1u;
+                }
+                // Stage this row of every partner's columns in the send slots (free again: the
+                // partners have consumed the previous tile's copies), then one bulk copy per partner
+                // moves the warp's 32 rows into the partner's slot for this CTA.
+                const uint32_t send_base = base + Cfg::kOffSend;
+#pragma unroll
+                for (uint32_t j = 0; j < uint32_t(KS); ++j) {
+                    if (j == ks_rank) continue;
+                    uint32_t v[W];
+                    slice(j, v);
+                    const uint32_t q = j < ks_rank ? j : j - 1u;  // send slot of partner j
+                    const uint32_t row_addr = send_base + q * uint32_t(Cfg::kRecvSlotBytes) + row_local * uint32_t(W * 4);
+#pragma unroll
+                    for (uint32_t c = 0; c < kChunks; ++c)
+                        ptx::st_shared_v4(row_addr + chunk_at(c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    constexpr uint32_t kWarpBytes = 32u * uint32_t(W * 4);  // a warp's 32 rows of one slot
+                    const uint32_t off = quarter * kWarpBytes;
+#pragma unroll
+                    for (uint32_t j = 0; j < uint32_t(KS); ++j) {
+                        if (j == ks_rank) continue;
+                        const uint32_t q = j < ks_rank ? j : j - 1u;
+                        const uint32_t slot = ks_rank < j ? ks_rank : ks_rank - 1u;  // this CTA's slot in CTA j
+                        ptx::bulk_copy_to_cluster(
+                            ptx::map_to_rank(recv_base + slot * uint32_t(Cfg::kRecvSlotBytes) + off, j),
+                            send_base + q * uint32_t(Cfg::kRecvSlotBytes) + off, kWarpBytes,
+                            ptx::map_to_rank(bar_recv_full, j));
+                    }
+                }
+                if (first_epi_thread) GEMM_TRACE(kTraceKsSent);
+                uint32_t own[W];
+                slice(ks_rank, own);
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_acc_empty(acc));  // the accumulator is free for the MMA
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                if (first_epi_thread) {
+                    ptx::mbar_arrive_expect_tx(bar_recv_full, uint32_t(KS - 1) * uint32_t(Cfg::kRecvSlotBytes));
+                    *reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffRecvArmed) = ks_tiles + 1u;
+                }
+                const bool recv_ok = wait_bounded<CS>(bar_recv_full, recv_phase, p, abort_flag, kErrWaitRecv);
+                if (!__all_sync(0xffffffffu, recv_ok)) return false;
+                recv_phase ^= 1u;
+                if (first_epi_thread) GEMM_TRACE(kTraceKsReceived);
+                ++ks_tiles;
+                if (first_epi_thread) *reinterpret_cast<volatile uint32_t *>(smem + Cfg::kOffRecvDone) = ks_tiles;
+                float sum[W];
+#pragma unroll
+                for (uint32_t r = 0; r < uint32_t(KS); ++r) {
+                    if (r == ks_rank) {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) sum[i] = r == 0 ? __uint_as_float(own[i]) : sum[i] + __uint_as_float(own[i]);
+                    } else {
+                        const uint32_t slot = r < ks_rank ? r : r - 1u;
+                        const uint32_t src = recv_base + slot * uint32_t(Cfg::kRecvSlotBytes) + row_local * uint32_t(W * 4);
+#pragma unroll
+                        for (uint32_t c = 0; c < kChunks; ++c) {
+                            const float4 x = ptx::ld_shared_f4(src + chunk_at(c));
+                            const float t[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sum[4 * c + e] = r == 0 ? t[e] : sum[4 * c + e] + t[e];
+                        }
+                    }
+                }
+                // Every warp has read its rows of the partners' slices: they may refill this CTA's
+                // receive slots (a next tile: the reads must be ordered before their copies, a
+                // cluster-scope release), or, after the last tile, exit (their copies out of the send
+                // slots completed before this CTA's receive barrier did: a plain signal suffices)
+                const bool next = tile + num_clusters < p.dp_tiles;
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (uint32_t j = 0; j < uint32_t(KS); ++j) {
+                        if (j == ks_rank) continue;
+                        if (next) ptx::mbar_arrive_cluster(ptx::map_to_rank(bar_peer_free, j));
+                        else ptx::mbar_arrive_cluster_signal(ptx::map_to_rank(bar_peer_free, j));
+                    }
+                }
+                const uint32_t row = row0 + lane;
+                const uint32_t col = col0 + ks_rank * uint32_t(W);
+                if (row < p.m) {
+                    __half *dst = static_cast<__half *>(p.c_out) + size_t(row) * p.n + col;
+#pragma unroll
+                    for (int g = 0; g < W / 8; ++g) {
+                        if (col + uint32_t(8 * g) >= p.n) break;
+                        const float *q = sum + 8 * g;
+                        ptx::st_global_v4(dst + 8 * g, pack_half2(__float_as_uint(q[0]), __float_as_uint(q[1])),
+                                          pack_half2(__float_as_uint(q[2]), __float_as_uint(q[3])),
+                                          pack_half2(__float_as_uint(q[4]), __float_as_uint(q[5])),
+                                          pack_half2(__float_as_uint(q[6]), __float_as_uint(q[7])));
+                    }
+                }
+                if (first_epi_thread) GEMM_TRACE(kTraceStored);
+                return true;
+            }
             // Partial-tile layout in the workspace: per warp quarter and 64-column chunk, 16 float4
             // slots x 32 lanes, so every warp-wide 16-byte access is one contiguous 512-byte run.
             const uint32_t piece = quarter * 32u * BN + lane * 4u;
@@ -854,6 +1069,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
             return true;
         });
         if (lane == 0) ptx::bulk_wait_group<0>();
+        if constexpr (KS > 1) {
+            // The partners have consumed this CTA's last slices: the bulk copies out of its send
+            // slots are complete, so the CTA may exit (bounded: after an abort the wait gives up)
+            if (ks_tiles > 0u) (void)wait_bounded<CS>(bar_peer_free, peer_phase, p, abort_flag, kErrWaitPeerFree);
+        }
         if (threadIdx.x == 64u) GEMM_TRACE(kTraceStoresDone);
     }
 
@@ -869,8 +1089,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     // barriers may read the other CTAs' flags: after an abort anywhere in the cluster they wait for
     // the ring loads still in flight before any CTA exits.
     if (threadIdx.x == 0 && (CG == 1 || leader))
-        nt_abort_drain<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI>(p);
-    if constexpr (CS > 1) ptx::cluster_sync();
+        nt_abort_drain<CG, BN, STAGES, MC, B_KMAJOR, C_F16, C_TRANS, EPI, KS>(p);
+    // (a K-split CTA's drain reads nothing of the other CTAs, and nothing of the cluster touches its
+    // shared memory once all have passed the barrier above: no second barrier)
+    if constexpr (CS > 1 && KS == 1) ptx::cluster_sync();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::kTmemCols);
     if (threadIdx.x == 32u) GEMM_TRACE(kTraceExit);
 }

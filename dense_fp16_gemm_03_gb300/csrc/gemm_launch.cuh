@@ -29,7 +29,14 @@ struct Variant {
     cudaError_t (*launch)(const gemm_f16_plan_t &, const KernelParams &, cudaStream_t);
     int threads;  // threads per CTA
     int b_box;    // B rows per TMA box (B [N,K] layout)
+    int ks;       // > 1: the K blocks of each tile split across a cluster of ks single CTAs
 };
+
+// CTAs per cluster
+int cluster_of(const Variant &var)
+{
+    return var.cg * var.mc * var.ks;
+}
 
 // Launch `kernel` persistently with clusters of `cs` CTAs, as a programmatic dependent launch.
 cudaError_t launch_persistent(const void *kernel, const gemm_f16_plan_t &plan, const KernelParams &params,
@@ -61,12 +68,12 @@ cudaError_t launch_persistent(const void *kernel, const gemm_f16_plan_t &plan, c
     return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
-template <int CG, int BN, int ST, int MC, bool BK, bool CF, bool CT, int EP>
+template <int CG, int BN, int ST, int MC, bool BK, bool CF, bool CT, int EP, int KS>
 cudaError_t launch_variant(const gemm_f16_plan_t &plan, const KernelParams &params, cudaStream_t stream)
 {
-    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP>),
+    return launch_persistent(reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP, KS>),
                              plan, params, stream, kNumThreads,
-                             KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes, CG * MC);
+                             KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP, KS>::kSmemBytes, CG * MC * KS);
 }
 
 template <int ST, int HN>
@@ -76,14 +83,15 @@ cudaError_t launch_wide(const gemm_f16_plan_t &plan, const KernelParams &params,
                              kWideThreads, WideCfg<ST, HN>::kSmemBytes, 2);
 }
 
-#define GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, EP)                                                        \
+#define GEMM_VARIANT_K(CG, BN, ST, MC, BK, CF, CT, EP, KS)                                                    \
     Variant                                                                                                   \
     {                                                                                                         \
-        CG, BN, ST, MC, (BK ? 0 : 1), (CT ? 1 : 0), KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kSmemBytes,    \
-            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP>),              \
-            &launch_variant<CG, BN, ST, MC, BK, CF, CT, EP>, kNumThreads,                                     \
-            KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP>::kBSlice                                                \
+        CG, BN, ST, MC, (BK ? 0 : 1), (CT ? 1 : 0), KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP, KS>::kSmemBytes, \
+            reinterpret_cast<const void *>(&gemm_f16_nt_kernel<CG, BN, ST, MC, BK, CF, CT, EP, KS>),          \
+            &launch_variant<CG, BN, ST, MC, BK, CF, CT, EP, KS>, kNumThreads,                                 \
+            KernelCfg<CG, BN, ST, MC, BK, CF, CT, EP, KS>::kBSlice, KS                                        \
     }
+#define GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, EP) GEMM_VARIANT_K(CG, BN, ST, MC, BK, CF, CT, EP, 1)
 #define GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, CT) GEMM_VARIANT_E(CG, BN, ST, MC, BK, CF, CT, 2)
 #define GEMM_VARIANT_L(CG, BN, ST, MC, BK, CF) GEMM_VARIANT_X(CG, BN, ST, MC, BK, CF, false)
 #define GEMM_VARIANT(CG, BN, ST, MC) GEMM_VARIANT_L(CG, BN, ST, MC, true, true)
@@ -92,7 +100,7 @@ cudaError_t launch_wide(const gemm_f16_plan_t &plan, const KernelParams &params,
     {                                                                                                          \
         2, WideCfg<ST, HN>::kBN, ST, 1, 0, 0, WideCfg<ST, HN>::kSmemBytes,                                     \
             reinterpret_cast<const void *>(&gemm_f16_nt_wide_kernel<ST, HN>), &launch_wide<ST, HN>,            \
-            kWideThreads, WideCfg<ST, HN>::kBBoxRows                                                           \
+            kWideThreads, WideCfg<ST, HN>::kBBoxRows, 1                                                        \
     }
 
 const Variant kVariants[] = {
@@ -120,6 +128,11 @@ const Variant kVariants[] = {
     GEMM_VARIANT_WIDE(5, 160),  // 17: 256 x 320, five stages (4096^3: 208 tiles, 2.7 waves, where 512 columns
                                 //     make 128 tiles, 1.7 waves)
     GEMM_VARIANT(1, 64, 8, 1),  // 18: 128 x 64 tile, one CTA (small, latency-bound products)
+    // K split: each tile's K blocks shared by a cluster of single CTAs, partials traded through
+    // distributed shared memory (products with fewer tiles than SMs)
+    GEMM_VARIANT_K(1, 64, 4, 1, true, true, false, 2, 4),   // 19: 128 x 64 tile on four CTAs
+    GEMM_VARIANT_K(1, 64, 6, 1, true, true, false, 2, 2),   // 20: 128 x 64 tile on two CTAs
+    GEMM_VARIANT_K(1, 128, 4, 1, true, true, false, 2, 2),  // 21: 128 x 128 tile on two CTAs
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
@@ -184,6 +197,7 @@ gemm_status_t encode_tensor_maps(const Variant &var, const gemm_f16_plan_t &plan
     // kernel-side problem: the transposed one for a swapped variant
     const void *ka = var.swap ? b : a;
     const void *kb = var.swap ? a : b;
+    params->c_out = c;
     const int64_t km = var.swap ? plan.n : plan.m;
     const int64_t kn = var.swap ? plan.m : plan.n;
     st = encode_matrix(enc, &params->tmap_a, ka, uint64_t(km), uint64_t(plan.k), kBlockK,
@@ -226,7 +240,7 @@ cudaError_t launch_split_reduce(const gemm_f16_plan_t &plan, const Variant &var,
     r.n = uint32_t(plan.n);
     r.split_k = uint32_t(plan.split_k);
     r.bn = uint32_t(var.bn);
-    r.cs = uint32_t(var.cg * var.mc);
+    r.cs = uint32_t(cluster_of(var));
     r.block_m = uint32_t(plan.block_m);
     r.block_n = uint32_t(plan.block_n);
     r.cta_rows = (var.cg == 1 && var.mc > 1) ? 0u : 128u;  // single CTAs sharing A sit along N

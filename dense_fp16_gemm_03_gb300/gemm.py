@@ -99,7 +99,7 @@ def lib():
         "gemm_f16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "gemm_f16_variant_count": (i32, []),
-        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32, pi32]),
+        "gemm_f16_variant_info": (ctypes.c_int, [i32, pi32, pi32, pi32, pi32, pi32, pi32, pi32, pi32]),
         "gemm_f16_nt_plan": (ctypes.c_int, [i64, i64, i64, P]),
         "gemm_f16_nt_plan_for": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, P]),
         "gemm_f16_nt_plan_for_clusters": (ctypes.c_int, [i64, i64, i64, i32, pi32, i32, i32, i32, i32, P]),
@@ -170,12 +170,13 @@ def gemm_f16_variant_count():
 
 
 def gemm_f16_variant_info(variant):
-    cg, bn, st, sm, cl, lay, sw = (ctypes.c_int32() for _ in range(7))
+    cg, bn, st, sm, cl, lay, sw, ks = (ctypes.c_int32() for _ in range(8))
     _check(lib().gemm_f16_variant_info(variant, ctypes.byref(cg), ctypes.byref(bn), ctypes.byref(st),
-                                       ctypes.byref(sm), ctypes.byref(cl), ctypes.byref(lay), ctypes.byref(sw)),
+                                       ctypes.byref(sm), ctypes.byref(cl), ctypes.byref(lay), ctypes.byref(sw),
+                                       ctypes.byref(ks)),
            "gemm_f16_variant_info")
     return {"cta_group": cg.value, "block_n": bn.value, "stages": st.value, "smem_bytes": sm.value,
-            "cluster": cl.value, "layout": lay.value, "swapped": sw.value}
+            "cluster": cl.value, "layout": lay.value, "swapped": sw.value, "k_split": ks.value}
 
 
 def gemm_f16_nt_plan(m, n, k):

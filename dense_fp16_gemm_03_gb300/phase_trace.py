@@ -23,7 +23,8 @@ from . import build as _build
 from . import gemm as G
 
 PHASES = ["entry", "set_up", "dep_wait", "first_full", "mma_done", "acc_ready", "stored", "stores_done",
-          "teardown", "exit"]
+          "teardown", "exit", "ks_sent", "ks_received"]
+COMMON = PHASES[:10]  # phases every traced plan passes (the last two are the K-split exchange's)
 SLOTS = 16
 
 
@@ -34,6 +35,8 @@ def _trace_lib():
     L.gemm_f16_nt_ws.argtypes = [i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.gemm_f16_trace_set.restype = None
     L.gemm_f16_trace_set.argtypes = [vp]
+    L.gemm_f16_nt_run.restype = ctypes.c_int
+    L.gemm_f16_nt_run.argtypes = [ctypes.POINTER(G.Plan), vp, vp, vp, vp, ctypes.c_size_t, vp]
     return L
 
 
@@ -52,7 +55,7 @@ def _replay_us(graph, stream, launches, reps=5):
     return statistics.median(ts)
 
 
-def trace_shape(m, n, k, launches=40, traced_at=20, seed=0):
+def trace_shape(m, n, k, launches=40, traced_at=20, seed=0, variant=-1):
     T = _trace_lib()
     P = G.lib()
     gen = torch.Generator(device="cuda").manual_seed(seed)
@@ -60,22 +63,22 @@ def trace_shape(m, n, k, launches=40, traced_at=20, seed=0):
     b = (torch.randint(-8, 9, (n, k), device="cuda", generator=gen).to(torch.float16) / 8)
     c_trace = torch.empty((m, n), dtype=torch.float16, device="cuda")
     c_prod = torch.empty((m, n), dtype=torch.float16, device="cuda")
-    plan = G.gemm_f16_nt_plan(m, n, k)
+    plan = G.gemm_f16_nt_plan(m, n, k) if variant < 0 else G.gemm_f16_nt_plan_ex(m, n, k, variant, 0, 0)
     ws = torch.empty(max(256, int(plan.workspace_bytes)), dtype=torch.uint8, device="cuda")
     bufs = [torch.zeros(plan.grid * SLOTS, dtype=torch.int64, device="cuda") for _ in range(3)]
     stream = torch.cuda.Stream()
 
     def call_trace():
-        st = T.gemm_f16_nt_ws(m, n, k, a.data_ptr(), b.data_ptr(), c_trace.data_ptr(), ws.data_ptr(),
-                              ws.numel(), stream.cuda_stream)
+        st = T.gemm_f16_nt_run(ctypes.byref(plan), a.data_ptr(), b.data_ptr(), c_trace.data_ptr(), ws.data_ptr(),
+                               ws.numel(), stream.cuda_stream)
         if st != 0:
-            raise G.GemmError(st, "gemm_f16_nt_ws (trace build)")
+            raise G.GemmError(st, "gemm_f16_nt_run (trace build)")
 
     def call_prod():
-        st = P.gemm_f16_nt_ws(m, n, k, a.data_ptr(), b.data_ptr(), c_prod.data_ptr(), ws.data_ptr(),
-                              ws.numel(), stream.cuda_stream)
+        st = P.gemm_f16_nt_run(ctypes.byref(plan), a.data_ptr(), b.data_ptr(), c_prod.data_ptr(), ws.data_ptr(),
+                               ws.numel(), stream.cuda_stream)
         if st != 0:
-            raise G.GemmError(st, "gemm_f16_nt_ws")
+            raise G.GemmError(st, "gemm_f16_nt_run")
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -128,6 +131,9 @@ def trace_shape(m, n, k, launches=40, traced_at=20, seed=0):
             monotone &= all(x <= y for x, y in zip(chain, chain[1:]))
             if v[9] != 0 and v[7] != 0:
                 monotone &= v[7] <= v[9]
+            # K split: accumulator ready, slices sent, partner slices received, stores issued
+            ks = [x for x in (v[5], v[10], v[11], v[6]) if x != 0]
+            monotone &= all(x <= y for x, y in zip(ks, ks[1:]))
         out["launches"].append(row)
     out["phases_in_order"] = monotone
     out["handover_us"] = [round(out["launches"][i + 1]["dep_wait"][0] - out["launches"][i]["exit"][1], 3)
@@ -139,10 +145,12 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("shapes", help="comma-separated MxNxK list")
     ap.add_argument("--launches", type=int, default=40)
+    ap.add_argument("--variants", default="-1", help="comma-separated variants (-1: the automatic plan)")
     args = ap.parse_args(argv)
     for spec in args.shapes.split(","):
         m, n, k = (int(x) for x in spec.split("x"))
-        print(json.dumps(trace_shape(m, n, k, launches=args.launches)), flush=True)
+        for v in args.variants.split(","):
+            print(json.dumps(trace_shape(m, n, k, launches=args.launches, variant=int(v))), flush=True)
 
 
 if __name__ == "__main__":

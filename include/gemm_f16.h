@@ -104,7 +104,7 @@ typedef struct gemm_f16_plan {
     int64_t dp_tiles;        /* tiles walked data-parallel (all of them when stream_k == 0) */
     int64_t sk_iters;        /* K-block iterations of the remaining tiles, split evenly over the clusters */
     int32_t grid;            /* CTAs launched (persistent: <= resident slots) */
-    int32_t cluster;         /* CTAs per cluster (cta_group times the multicast width) */
+    int32_t cluster;         /* CTAs per cluster (cta_group times the multicast width times the K split) */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t num_sms;         /* SM count the plan was made for */
     uint64_t workspace_bytes;/* device workspace the plan needs (0 = none) */
@@ -154,15 +154,19 @@ const char *gemm_status_string(gemm_status_t status);
 /* Number of compiled kernel variants, and the shape of one of them: CTAs
  * per MMA (cta_group), tile N of one CTA or pair (a wide tile's two MMAs
  * together), ring depth, dynamic shared memory, CTAs
- * per cluster, layout (as in gemm_f16_plan_t) and whether it computes the
+ * per cluster, layout (as in gemm_f16_plan_t), whether it computes the
  * transposed product C^T = B . A^T with the operands swapped (for products
  * with few rows of A; a plan of such a variant has tiles_m over n and
- * tiles_n over m).  Any pointer may be NULL.  Returns GEMM_ERR_INVALID_ARG
- * for an index out of range. */
+ * tiles_n over m), and its K split: 1, or the number of single CTAs of a
+ * cluster that share each 128 x block_n tile, each accumulating one run of
+ * its K blocks before they add the partials through distributed shared
+ * memory (data-parallel plans only: no stream-K tail, no split-K).  Any
+ * pointer may be NULL.  Returns GEMM_ERR_INVALID_ARG for an index out of
+ * range. */
 int32_t gemm_f16_variant_count(void);
 gemm_status_t gemm_f16_variant_info(int32_t variant, int32_t *cta_group, int32_t *block_n,
                                     int32_t *stages, int32_t *smem_bytes, int32_t *cluster,
-                                    int32_t *layout, int32_t *swapped);
+                                    int32_t *layout, int32_t *swapped, int32_t *k_split);
 
 /*
  * Plan for the current CUDA device: validates the shape, checks the device
@@ -367,7 +371,9 @@ gemm_status_t gemm_f16_nt_run_stall_test(const gemm_f16_plan_t *plan, const void
  * zeroes the buffer) was not reached; give one buffer per traced launch.
  * Phases 0..9: kernel entry; set-up done; previous launch complete; a tile's
  * first ring stage full; its MMAs committed; its accumulator ready; its
- * stores issued; all bulk stores complete; teardown barrier; exit.  The
+ * stores issued; all bulk stores complete; teardown barrier; exit; for the
+ * K-split variants also 10: a tile's partner slices sent, 11: the
+ * partners' slices of it received.  The
  * buffer is owned by the caller and
  * must hold grid * 16 slots and stay allocated until the traced launches
  * have completed.  The wide-tile kernel is not traced.  The pointer is

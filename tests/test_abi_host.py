@@ -306,6 +306,12 @@ def _segments(p):
 def test_stream_k_covers_every_k_block_once(L, shape):
     m, n, k = shape
     for variant in range(G.gemm_f16_variant_count()):
+        if G.gemm_f16_variant_info(variant)["k_split"] > 1:
+            # a K-split cluster already shares every tile's K blocks: no stream-K tail, no split-K
+            for stream_k in (1, 2):
+                with pytest.raises(G.GemmError):
+                    G.gemm_f16_nt_plan_for(m, n, k, 152, 0, variant, 0, stream_k)
+            continue
         p = G.gemm_f16_nt_plan_for(m, n, k, 152, 0, variant, 0, 1)
         if not p.stream_k:
             continue
@@ -370,7 +376,10 @@ def test_k_rotation_rule(L):
     ((128, 8192, 8192), 1, 0, True),       # 32 pair tiles would idle most pairs: 128 x 128 tiles, K split
     ((256, 256, 1 << 20), 2, 0, True),     # one tile, long K: split-K over every cluster
     ((512, 512, 65536), 4, 0, True),
-    ((200, 1000, 3000), 2, 0, True),       # few tiles: split-K rather than a tail without a whole wave
+    ((200, 1000, 3000), 19, 0, False),     # few tiles, 47 K blocks: each tile's K shared by a cluster of four
+    ((256, 256, 8192), 2, 0, True),        # one pair tile, 128 K blocks: split-K (unsplit it ran on two SMs)
+    ((512, 512, 1024), 20, 0, False),      # 16 K blocks, tiles for half the pairs: K split over CTA pairs
+    ((1024, 1024, 2048), 21, 0, False),    # 32 K blocks, 128 x 128 tiles for 64 of 76 pairs: K split in two
     ((4096, 4096, 4096), 4, 1, False),     # whole waves in front: a stream-K tail over every cluster
 ])
 def test_auto_variant_choices(L, shape, variant, stream_k, split):

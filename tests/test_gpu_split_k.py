@@ -77,7 +77,7 @@ def test_split_k_refused_where_unsupported():
     for v in range(G.gemm_f16_variant_count()):
         info = G.gemm_f16_variant_info(v)
         capable = (info["layout"] == 0 and not info["swapped"] and info["block_n"] % 64 == 0
-                   and info["block_n"] <= 256)
+                   and info["block_n"] <= 256 and info["k_split"] == 1)
         if capable:
             assert G.gemm_f16_nt_plan_ex(1000, 1000, 1000, v, 0, 2).split_k >= 2
         else:

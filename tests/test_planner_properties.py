@@ -98,8 +98,10 @@ def test_random_plans_are_runnable(L):
         try:
             p = G.gemm_f16_nt_plan_for_clusters(m, n, k, 152, clusters, variant, int(rng.integers(0, 9)), stream_k)
         except G.GemmError as e:
-            # only a split requested of a variant without split K is refused
-            assert e.status == G.GEMM_ERR_INVALID_ARG and stream_k == 2
+            # only a split requested of a variant without split K is refused, and a stream-K tail of a
+            # variant whose clusters split every tile's K blocks
+            k_split = variant >= 0 and G.gemm_f16_variant_info(variant)["k_split"] > 1
+            assert e.status == G.GEMM_ERR_INVALID_ARG and (stream_k == 2 or (stream_k == 1 and k_split))
             continue
         assert (p.m, p.n, p.k) == (m, n, k)
         _check_plan(p, m, n, k, clusters)
