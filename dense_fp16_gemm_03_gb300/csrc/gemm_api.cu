@@ -631,24 +631,16 @@ gemm_status_t run_plan(const gemm_f16_plan_t &plan, const void *a, const void *b
     return launch_plan(plan, dev, a, b, c, ws, ws_bytes, stream, skip_fill, wait_limit);
 }
 
-gemm_status_t launch_plan(const gemm_f16_plan_t &plan, const DeviceInfo *dev, const void *a, const void *b, void *c,
-                          void *ws, size_t ws_bytes, cudaStream_t stream, uint32_t skip_fill, long long wait_limit)
+// The kernel parameters of one launch of `plan` (k > 0): workspace and pointer checks, the tensor
+// maps and the schedule; everything but the stream-K stamp, which every launch draws afresh.
+gemm_status_t build_params(const gemm_f16_plan_t &plan, const DeviceInfo *dev, const void *a, const void *b, void *c,
+                           void *ws, size_t ws_bytes, uint32_t skip_fill, long long wait_limit, KernelParams *params)
 {
-    if (plan.m == 0 || plan.n == 0) return GEMM_OK;
     if (plan.workspace_bytes > 0) {
         if (ws == nullptr || ws_bytes < plan.workspace_bytes) return GEMM_ERR_WORKSPACE;
         if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GEMM_ERR_ALIGNMENT;
     }
     const Variant &var = kVariants[plan.variant];
-    if (plan.k == 0) {
-        const size_t c_elem = var.layout == 1 ? 4u : 2u;
-        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * c_elem, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-        return GEMM_OK;
-    }
-    gemm_status_t st = GEMM_OK;
     if (var.mc > 1) {
         // Cluster multicast loads deliver one copy of a tile to several CTAs of this GPU; they are
         // only used on this GPU's own device memory (never on a peer's or on host-mapped memory).
@@ -662,48 +654,73 @@ gemm_status_t launch_plan(const gemm_f16_plan_t &plan, const DeviceInfo *dev, co
             if (at.type != cudaMemoryTypeDevice || at.device != cur) return GEMM_ERR_INVALID_ARG;
         }
     }
-
-    KernelParams params;
-    memset(&params, 0, sizeof(params));
-    st = encode_tensor_maps(var, plan, a, b, c, &params);
-#ifdef GEMM_F16_PHASE_TRACE
-    params.trace = g_trace_buffer.load();
-#endif
+    memset(params, 0, sizeof(*params));
+    gemm_status_t st = encode_tensor_maps(var, plan, a, b, c, params);
     if (st != GEMM_OK) return st;
     // kernel-side problem: the transposed one for a swapped variant
     const int64_t km = var.swap ? plan.n : plan.m;
     const int64_t kn = var.swap ? plan.m : plan.n;
-    params.raster = make_raster(uint32_t(plan.tiles_m), uint32_t(plan.tiles_n), uint32_t(plan.raster_width));
-    params.m = uint32_t(km);
-    params.n = uint32_t(kn);
-    params.k = uint32_t(plan.k);
-    params.num_tiles = uint32_t(plan.num_tiles);
-    params.k_blocks = uint32_t(plan.k_blocks);
-    params.dp_tiles = uint32_t(plan.dp_tiles);
-    params.k_rotate = plan.k_rotate ? 1u : 0u;
-    params.sk_iters = uint64_t(plan.sk_iters);
+    params->raster = make_raster(uint32_t(plan.tiles_m), uint32_t(plan.tiles_n), uint32_t(plan.raster_width));
+    params->m = uint32_t(km);
+    params->n = uint32_t(kn);
+    params->k = uint32_t(plan.k);
+    params->num_tiles = uint32_t(plan.num_tiles);
+    params->k_blocks = uint32_t(plan.k_blocks);
+    params->dp_tiles = uint32_t(plan.dp_tiles);
+    params->k_rotate = plan.k_rotate ? 1u : 0u;
+    params->sk_iters = uint64_t(plan.sk_iters);
     if (plan.split_k > 1) {
-        params.split_k = uint32_t(plan.split_k);
-        params.partials = static_cast<float *>(ws);
+        params->split_k = uint32_t(plan.split_k);
+        params->partials = static_cast<float *>(ws);
     }
     if (plan.stream_k) {
-        params.partials = static_cast<float *>(ws);
-        params.flags = reinterpret_cast<uint64_t *>(static_cast<char *>(ws) +
-                                                    streamk_partials_bytes(plan.grid, var.bn));
-        params.sk_stamp = next_sk_stamp();
+        params->partials = static_cast<float *>(ws);
+        params->flags = reinterpret_cast<uint64_t *>(static_cast<char *>(ws) +
+                                                     streamk_partials_bytes(plan.grid, var.bn));
     }
-    params.skip_fill = skip_fill;
-    params.wait_limit = wait_limit;
-    params.error_word = dev->error_word;
+    params->skip_fill = skip_fill;
+    params->wait_limit = wait_limit;
+    params->error_word = dev->error_word;
+    return GEMM_OK;
+}
+
+// Launch `plan` with parameters from build_params (a fresh stream-K stamp when it has a tail), and its
+// split-K reduction.
+gemm_status_t launch_params(const gemm_f16_plan_t &plan, KernelParams &params, void *c, cudaStream_t stream)
+{
+    const Variant &var = kVariants[plan.variant];
+    if (plan.stream_k) params.sk_stamp = next_sk_stamp();
+#ifdef GEMM_F16_PHASE_TRACE
+    params.trace = g_trace_buffer.load();
+#endif
     if (var.launch(plan, params, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    if (plan.split_k > 1 && launch_split_reduce(plan, var, params.raster, ws, c, stream) != cudaSuccess) {
+    if (plan.split_k > 1 && launch_split_reduce(plan, var, params.raster, params.partials, c, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
     return GEMM_OK;
+}
+
+gemm_status_t launch_plan(const gemm_f16_plan_t &plan, const DeviceInfo *dev, const void *a, const void *b, void *c,
+                          void *ws, size_t ws_bytes, cudaStream_t stream, uint32_t skip_fill, long long wait_limit)
+{
+    if (plan.m == 0 || plan.n == 0) return GEMM_OK;
+    if (plan.k == 0) {
+        if (plan.workspace_bytes > 0 && (ws == nullptr || ws_bytes < plan.workspace_bytes)) return GEMM_ERR_WORKSPACE;
+        const size_t c_elem = kVariants[plan.variant].layout == 1 ? 4u : 2u;
+        if (cudaMemsetAsync(c, 0, size_t(plan.m) * size_t(plan.n) * c_elem, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        return GEMM_OK;
+    }
+    KernelParams params;
+    gemm_status_t st = build_params(plan, dev, a, b, c, ws, ws_bytes, skip_fill, wait_limit, &params);
+    if (st != GEMM_OK) return st;
+    return launch_params(plan, params, c, stream);
 }
 
 // A wait may legitimately last one whole tile's main loop: allow ~1 s plus
@@ -800,6 +817,62 @@ gemm_status_t device_plan(int64_t m, int64_t n, int64_t k, int32_t variant, int3
     if (st != GEMM_OK) return st;
     if (dev_out) *dev_out = dev;
     return make_plan(m, n, k, dev->num_sms, 0, variant, raster_width, stream_k, out, dev->max_clusters, layout);
+}
+
+// Launches of the automatic entry points repeat: a caller runs the same shapes on the same buffers
+// step after step.  Each host thread keeps its last few launches -- plan and encoded parameters --
+// keyed on the context, the entry point, the shape, every pointer and the workspace size, so that a
+// repeat skips planning and the tensor-map encodes (the parameters depend on nothing else; the
+// stream-K stamp is drawn again at every launch).
+struct LaunchCacheEntry {
+    bool valid;
+    int entry;  // 0: gemm_f16_nt, 1: gemm_f16_nt_ws
+    unsigned long long ctx;
+    int64_t m, n, k;
+    const void *a, *b;
+    void *c, *ws;
+    size_t ws_bytes;
+    gemm_f16_plan_t plan;
+    KernelParams params;
+};
+constexpr int kLaunchCacheEntries = 4;
+thread_local LaunchCacheEntry t_launch_cache[kLaunchCacheEntries];
+thread_local int t_launch_cache_next = 0;
+
+// The automatic plan of (m, n, k) launched on a, b, c (m, n, k > 0, arguments already checked).
+gemm_status_t launch_auto(int entry, int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *c, void *ws,
+                          size_t ws_bytes, cudaStream_t stream)
+{
+    unsigned long long ctx = 0;
+    gemm_status_t st = current_context_id(&ctx);
+    if (st != GEMM_OK) return st;
+    for (LaunchCacheEntry &e : t_launch_cache) {
+        if (e.valid && e.entry == entry && e.ctx == ctx && e.m == m && e.n == n && e.k == k && e.a == a &&
+            e.b == b && e.c == c && e.ws == ws && e.ws_bytes == ws_bytes)
+            return launch_params(e.plan, e.params, c, stream);
+    }
+    gemm_f16_plan_t p;
+    DeviceInfo *dev = nullptr;
+    st = device_plan(m, n, k, -1, 0, entry == 0 ? 0 : -1, &p, 0, &dev);
+    if (st != GEMM_OK) return st;
+    LaunchCacheEntry &e = t_launch_cache[t_launch_cache_next];
+    e.valid = false;
+    st = build_params(p, dev, a, b, c, ws, ws_bytes, ~0u, default_wait_limit(p.k_blocks), &e.params);
+    if (st != GEMM_OK) return st;
+    e.entry = entry;
+    e.ctx = dev->ctx_id;
+    e.m = m;
+    e.n = n;
+    e.k = k;
+    e.a = a;
+    e.b = b;
+    e.c = c;
+    e.ws = ws;
+    e.ws_bytes = ws_bytes;
+    e.plan = p;
+    e.valid = true;
+    t_launch_cache_next = (t_launch_cache_next + 1) % kLaunchCacheEntries;
+    return launch_params(e.plan, e.params, c, stream);
 }
 
 // ---------------------------------------------- host-buffer pipeline
@@ -920,12 +993,15 @@ gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, con
     st = check_pointers(m, n, k, a, b, c);
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
-    gemm_f16_plan_t p;
-    DeviceInfo *dev = nullptr;
-    st = device_plan(m, n, k, -1, 0, -1, &p, 0, &dev);
-    if (st != GEMM_OK) return st;
-    return launch_plan(p, dev, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
-                       default_wait_limit(p.k_blocks));
+    if (k == 0) {
+        gemm_f16_plan_t p;
+        DeviceInfo *dev = nullptr;
+        st = device_plan(m, n, k, -1, 0, -1, &p, 0, &dev);
+        if (st != GEMM_OK) return st;
+        return launch_plan(p, dev, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                           default_wait_limit(p.k_blocks));
+    }
+    return launch_auto(1, m, n, k, a, b, c, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const void *b, void *c,
@@ -936,12 +1012,15 @@ gemm_status_t gemm_f16_nt(int64_t m, int64_t n, int64_t k, const void *a, const 
     st = check_pointers(m, n, k, a, b, c);
     if (st != GEMM_OK) return st;
     if (m == 0 || n == 0) return GEMM_OK;
-    gemm_f16_plan_t p;
-    DeviceInfo *dev = nullptr;
-    st = device_plan(m, n, k, -1, 0, 0, &p, 0, &dev);
-    if (st != GEMM_OK) return st;
-    return launch_plan(p, dev, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream), ~0u,
-                       default_wait_limit(p.k_blocks));
+    if (k == 0) {
+        gemm_f16_plan_t p;
+        DeviceInfo *dev = nullptr;
+        st = device_plan(m, n, k, -1, 0, 0, &p, 0, &dev);
+        if (st != GEMM_OK) return st;
+        return launch_plan(p, dev, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream), ~0u,
+                           default_wait_limit(p.k_blocks));
+    }
+    return launch_auto(0, m, n, k, a, b, c, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c, void *workspace,

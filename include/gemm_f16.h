@@ -26,7 +26,13 @@
  * device address, the copy streams of gemm_f16_nt_host) is kept for the
  * context it was made in and made again when the current context changes,
  * so a cudaDeviceReset between calls is safe; a reset that races with a
- * call on another thread is not.
+ * call on another thread is not.  gemm_f16_nt and gemm_f16_nt_ws also keep,
+ * per host thread, their last four launches (plan and encoded kernel
+ * parameters), keyed on the context, the shape, the pointers a, b, c and
+ * the workspace and its size: a call that repeats one of them launches it
+ * again without planning and encoding (it reads nothing else; a buffer
+ * freed and allocated again at the same address with the same shape is the
+ * same launch).
  *
  * One GPU per call: a, b and c are memory of the current device.  The
  * variants that share one operand tile between the CTAs of a cluster by
