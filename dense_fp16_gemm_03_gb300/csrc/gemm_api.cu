@@ -366,6 +366,16 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
     if (short_k && cdiv(m, 128) * cdiv(n, 64) <= int64_t(num_sms)) return 18;
     if (short_k && cdiv(m, 128) * cdiv(n, 128) <= int64_t(num_sms)) return 1;
     if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
+    // Few tiles and more than 64 K blocks: the single-CTA 128 x 128 tile, its K split over the SMs,
+    // up to 4096 tile-K-blocks in all.  Device time per launch on GB300 (CUDA graph; this choice /
+    // the pair or multicast tile with split K chosen before): 256 x 256 x 8192 9.93 / 11.54 us,
+    // 256 x 256 x 32768 12.83 / 16.99, 512 x 512 x 8192 13.09 / 16.75, 512 x 256 x 16384 11.08 / 15.88,
+    // 384 x 384 x 16384 12.89 / 16.38, 256 x 1024 x 16384 17.07 / 19.32.  Beyond (512 x 512 x 32768
+    // 24.84 / 23.92) or with more tiles (768 x 768 x 8192 17.07 / 16.21) the larger tiles win.
+    {
+        const int64_t tiles128 = cdiv(m, 128) * cdiv(n, 128);
+        if (k_blocks > 64 && tiles128 <= 16 && tiles128 * k_blocks <= 4096) return 1;
+    }
     const int64_t pair_tiles_m = cdiv(m, 256), tiles_n = cdiv(n, 256);
     // Mid-size products (up to 32 K blocks) whose 256 x 256 pair tiles would not fill one wave: the
     // smallest single-CTA tile that still fits one wave, data-parallel.  Device time per launch on

@@ -377,7 +377,9 @@ def test_k_rotation_rule(L):
     ((256, 256, 1 << 20), 2, 0, True),     # one tile, long K: split-K over every cluster
     ((512, 512, 65536), 4, 0, True),
     ((200, 1000, 3000), 19, 0, False),     # few tiles, 47 K blocks: each tile's K shared by a cluster of four
-    ((256, 256, 8192), 2, 0, True),        # one pair tile, 128 K blocks: split-K (unsplit it ran on two SMs)
+    ((256, 256, 8192), 1, 0, True),        # four 128 x 128 tiles, 128 K blocks: split-K (unsplit it ran on two SMs)
+    ((512, 256, 16384), 1, 0, True),       # 8 tiles x 256 K blocks: 128 x 128 tiles with split-K
+    ((512, 512, 32768), 4, 0, True),       # 16 tiles x 512 K blocks: past 4096, multicast pairs with split-K
     ((512, 512, 1024), 20, 0, False),      # 16 K blocks, tiles for half the pairs: K split over CTA pairs
     ((1024, 1024, 2048), 21, 0, False),    # 32 K blocks, 128 x 128 tiles for 64 of 76 pairs: K split in two
     ((4096, 4096, 4096), 4, 1, False),     # whole waves in front: a stream-K tail over every cluster
