@@ -249,7 +249,9 @@ gemm_status_t gemm_f16_nt_ws(int64_t m, int64_t n, int64_t k, const void *a, con
 
 /* Launch a given plan (from any plan query, made for the current device's
  * SM count; either layout, c then being the plan's C or D).  The plan is
- * re-validated.  Computes the product of "1. WGMMA", "The Full Kernel" (or,
+ * re-validated (GEMM_ERR_INVALID_ARG for a plan this library would not
+ * make for its shape, e.g. a stream-K tail or split K on a K-split
+ * variant).  Computes the product of "1. WGMMA", "The Full Kernel" (or,
  * for layout 1, of "wgmma_gemm.cu"); the plan's fields only choose how. */
 gemm_status_t gemm_f16_nt_run(const gemm_f16_plan_t *plan, const void *a, const void *b, void *c,
                               void *workspace, size_t ws_bytes, gemm_stream_t stream);
