@@ -534,6 +534,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) GEMM_TRACE(kTraceSetUp);
+    bool arrived = false;  // K split: this thread has already arrived on the teardown's cluster barrier
 
     // Where this CTA's boxes of a segment start: the A rows m0, the B rows (or, B stored [K, N], the
     // columns) n0, and the K-walk rotation.  With k_rotate, a whole tile walks its K blocks from a
@@ -871,6 +872,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                         else ptx::mbar_arrive_cluster_signal(ptx::map_to_rank(bar_peer_free, j));
                     }
                 }
+                if (!next) {
+                    // This warp touches no other CTA's shared memory from here on: arrive on the
+                    // teardown's cluster barrier now (the release covers the copies and signals above),
+                    // so that its latency overlaps the stores of C instead of waiting for them.
+                    __syncwarp();
+                    ptx::tc_fence_before_sync();
+                    ptx::cluster_arrive_release();
+                    arrived = true;
+                }
                 const uint32_t row = row0 + lane;
                 const uint32_t col = col0 + ks_rank * uint32_t(W);
                 if (row < p.m) {
@@ -1081,8 +1091,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
     ptx::griddep_launch_dependents();  // a CTA whose epilogue stored nothing still lets the next launch in
     __syncwarp();
     ptx::tc_fence_before_sync();
-    if constexpr (CS > 1) ptx::cluster_sync();
-    else __syncthreads();
+    if constexpr (KS > 1) {
+        if (!arrived) ptx::cluster_arrive_release();  // (arrived: K-split epilogue warps after their last tile)
+        ptx::cluster_wait_acquire();
+    } else if constexpr (CS > 1) {
+        ptx::cluster_sync();
+    } else {
+        __syncthreads();
+    }
     ptx::tc_fence_after_sync();
     if (threadIdx.x == 0) GEMM_TRACE(kTraceTeardown);
     // Between two cluster barriers every CTA of the cluster is still running, so the owners of full

@@ -154,6 +154,18 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for a thread that has work left between its arrival (which
+// releases its earlier memory operations cluster-wide) and its wait.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // -------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)

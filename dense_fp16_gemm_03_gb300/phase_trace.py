@@ -122,18 +122,23 @@ def trace_shape(m, n, k, launches=40, traced_at=20, seed=0, variant=-1):
             if hit.numel() == 0:
                 continue
             row[name] = [round((int(hit.min()) - t0) / 1e3, 3), round((int(hit.max()) - t0) / 1e3, 3)]
-        # per CTA, the phases it reached come in causal order: entry .. teardown are each passed
-        # after the one before; exit (thread 32 frees tensor memory after the teardown barrier) is
-        # only ordered after the stores completed, not after thread 0's teardown stamp
+        # per CTA, the phases it reached come in causal order.  Without a K split: entry .. teardown
+        # each after the one before, and exit (thread 32 frees tensor memory after the teardown
+        # barrier) after the stores completed, not necessarily after thread 0's teardown stamp.  With
+        # one, the epilogue warps arrive on the teardown barrier right after the partner slices are in
+        # and only then store C: accumulator ready, slices sent, slices received, stored, stores done
+        # in order, and teardown and exit after the slices were received
         for cta in range(plan.grid):
             v = [int(x) for x in s[cta, :len(PHASES)].tolist()]
-            chain = [x for x in v[:9] if x != 0]
-            monotone &= all(x <= y for x, y in zip(chain, chain[1:]))
-            if v[9] != 0 and v[7] != 0:
-                monotone &= v[7] <= v[9]
-            # K split: accumulator ready, slices sent, partner slices received, stores issued
-            ks = [x for x in (v[5], v[10], v[11], v[6]) if x != 0]
-            monotone &= all(x <= y for x, y in zip(ks, ks[1:]))
+            if v[10] == 0 and v[11] == 0:
+                chain = [x for x in v[:9] if x != 0]
+                monotone &= all(x <= y for x, y in zip(chain, chain[1:]))
+                if v[9] != 0 and v[7] != 0:
+                    monotone &= v[7] <= v[9]
+            else:
+                chain = [x for x in (v[0], v[1], v[2], v[3], v[4], v[5], v[10], v[11], v[6], v[7]) if x != 0]
+                monotone &= all(x <= y for x, y in zip(chain, chain[1:]))
+                monotone &= all(v[11] <= x for x in (v[8], v[9]) if x != 0)
         out["launches"].append(row)
     out["phases_in_order"] = monotone
     out["handover_us"] = [round(out["launches"][i + 1]["dep_wait"][0] - out["launches"][i]["exit"][1], 3)
