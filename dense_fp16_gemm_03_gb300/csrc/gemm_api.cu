@@ -359,10 +359,15 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
         // (one strip of A rows keeps its split K over more SMs: 100 x 5000 x 3000 12.86 against 13.65 us)
         if (k_blocks >= 32 && m > 128 && tiles128 <= slots_of(21)) return 21;
     }
+    // (128 x 32 tiles, variant 22, wherever twice as many tiles still fit one wave: each SM then takes in
+    // 20 KB per K block against 24 KB; 256^3 3.00 against 3.21 us, 128^3 2.38 against 2.65, 512^3 4.08
+    // against 4.30, 512 x 512 x 256 3.07 against 3.28)
     if (m <= 128) {
+        if (short_k && cdiv(n, 32) <= int64_t(num_sms)) return 22;
         if (short_k && cdiv(n, 64) <= int64_t(num_sms)) return 18;
         return 2 * cdiv(n, 256) >= slots_of(13) ? 13 : 1;
     }
+    if (short_k && cdiv(m, 128) * cdiv(n, 32) <= int64_t(num_sms)) return 22;
     if (short_k && cdiv(m, 128) * cdiv(n, 64) <= int64_t(num_sms)) return 18;
     if (short_k && cdiv(m, 128) * cdiv(n, 128) <= int64_t(num_sms)) return 1;
     if (n <= 128) return 3;  // a 256-column tile would be half empty: the 256 x 128 pair tile
@@ -383,7 +388,7 @@ int32_t auto_variant(int64_t m, int64_t n, int64_t k_blocks, int32_t num_sms, co
     // chosen before): 512^3 4.39 / 4.84 / 6.95 us, 1024^3 6.91 / 6.89 / 13.09, 1536^3 9.56 / 9.96 /
     // 18.46, 2048^3 13.30 / 15.20 / 15.42, 1024 x 2048 x 512 5.25 / 5.74 / 7.02.
     if (k_blocks <= 32 && pair_tiles_m * tiles_n < slots_of(2)) {
-        for (int32_t v : {18, 1, 0})
+        for (int32_t v : {22, 18, 1, 0})
             if (cdiv(m, 128) * cdiv(n, kVariants[v].bn) <= int64_t(num_sms)) return v;
     }
     int32_t alt = 2;

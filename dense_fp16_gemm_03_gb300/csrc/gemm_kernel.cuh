@@ -166,7 +166,7 @@ struct KernelCfg {
     static_assert(KS == 1 || KS == 2 || KS == 4, "K split across the cluster");
     static_assert(KS == 1 || (CG == 1 && MC == 1 && B_KMAJOR && C_F16 && !C_TRANS), "K split: single-CTA fp16 tiles");
     static constexpr bool kAMC = (CG == 1 && MC > 1);  // single CTAs along N share A by multicast
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile N");
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
     static constexpr int kFullChunks = BN / 64;      // 64-column epilogue chunks
     static constexpr bool kTail = (BN % 64) != 0;   // plus one 32-column chunk
     static constexpr int kCS = CG * MC * KS;        // CTAs per cluster

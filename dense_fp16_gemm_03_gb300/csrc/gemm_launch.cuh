@@ -133,6 +133,7 @@ const Variant kVariants[] = {
     GEMM_VARIANT_K(1, 64, 4, 1, true, true, false, 2, 4),   // 19: 128 x 64 tile on four CTAs
     GEMM_VARIANT_K(1, 64, 6, 1, true, true, false, 2, 2),   // 20: 128 x 64 tile on two CTAs
     GEMM_VARIANT_K(1, 128, 4, 1, true, true, false, 2, 2),  // 21: 128 x 128 tile on two CTAs
+    GEMM_VARIANT(1, 32, 8, 1),  // 22: 128 x 32 tile, one CTA (small products: 20 KB per K block into each SM)
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
