@@ -874,8 +874,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_nt_kernel(const __gri
                 }
                 if (!next) {
                     // This warp touches no other CTA's shared memory from here on: arrive on the
-                    // teardown's cluster barrier now (the release covers the copies and signals above),
-                    // so that its latency overlaps the stores of C instead of waiting for them.
+                    // teardown's cluster barrier now, so that its latency overlaps the stores of C
+                    // instead of waiting for them.  The release covers the signals above; the bulk
+                    // copies have landed before any partner arrives (each waits for them first).
                     __syncwarp();
                     ptx::tc_fence_before_sync();
                     ptx::cluster_arrive_release();
